@@ -1,0 +1,545 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on one GB300 per rank.
+
+A step is one decode step of the batched GQA workload (32 requests, 32 query
+heads over 8 kv heads, head_dim 128, bf16, contexts uniform in [512, 4096],
+262144-slot pool, layer 2 of 4): the cache write of the 32 new K/V rows
+followed by paged decode attention (split kernel + merge) through
+req_to_token.  `value` is the step's algorithmic HBM bytes / step time (KV
+GB/s); the line also reports decode tokens/s, the decode kernel's roofline,
+the ragged-prefill TFLOP/s, the B=1 32K-context decode, an end-to-end figure
+through the public API with host buffers, and the fp64 oracle timed on the
+host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the workload (the path shards by request with no exchange), `value` is the
+sum over ranks of the bytes divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+L2_FLUSH_BYTES = 256 << 20        # > 2x the 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--chunk", type=int, default=0, help="decode split size (0: automatic)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the prefill / long-context / e2e / cpu legs")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        d = {}
+
+    def pick(*keys):
+        for k in keys:
+            v = d.get(k)
+            if isinstance(v, (int, float)) and v > 0:
+                return float(v)
+        return None
+    hbm = pick("hbm_gbs")
+    bf16 = pick("bf16_tflops")
+    bf16s = pick("bf16_tflops_sustained")
+    return {
+        "hbm_gbs": hbm or FALLBACK_HBM_GBS,
+        "hbm_source": "measured" if hbm else "fallback",
+        "bf16_tflops": bf16 or FALLBACK_BF16_TFLOPS,
+        "bf16_source": "measured" if bf16 else "fallback",
+        "bf16_tflops_sustained": bf16s or FALLBACK_BF16_TFLOPS_SUSTAINED,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def profile_traffic(name: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if the kernel
+    source changed since it was captured (the summary records its sha256)."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "paged_kv_cache_loc_gb300", "csrc", source)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if fields.get("source_sha256") != digest or "traffic_bytes_per_launch" not in fields:
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (the figures the rooflines use)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(case) -> float:
+    """K and V rows read + slot indices + q read + o written."""
+    eb = case.elem_bytes
+    tokens = float(case.seq_lens.sum())
+    row = case.n_kv_heads * case.head_dim * eb
+    return tokens * 2 * row + tokens * 4 + 2.0 * case.batch * case.n_heads * case.head_dim * eb
+
+
+def kv_write_bytes(case) -> float:
+    """New K and V rows read and written + write locations."""
+    n = float(case.out_cache_loc.size)
+    row = case.n_kv_heads * case.head_dim * case.elem_bytes
+    return n * 2 * row * 2 + n * 4
+
+
+def prefill_flops(case) -> float:
+    """4 * d * H * (causal query-key pairs): QK^T and PV over unmasked pairs."""
+    ql = case.q_lens.astype(np.float64)
+    pre = case.seq_lens.astype(np.float64) - ql
+    pairs = float(np.sum(ql * pre + ql * (ql + 1) / 2))
+    return 4.0 * case.head_dim * case.n_heads * pairs
+
+
+# ---------------------------------------------------------------------------
+# the pkv arm
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    """Pre-marshalled C-ABI calls for one decode step (kv_write + paged_decode)."""
+
+    def __init__(self, lib, cache, q, kn, vn, o, ws, layer_id, chunk, stream):
+        from paged_kv_cache_loc_gb300 import _lib
+        self.lib = lib
+        self.c = cache.c_struct()
+        self.cref = ctypes.byref(self.c)
+        self.layer = layer_id
+        self.k, self.v = ctypes.c_void_p(kn.data_ptr()), ctypes.c_void_p(vn.data_ptr())
+        self.n_new = int(kn.shape[0])
+        self.q, self.o = ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(o.data_ptr())
+        self.heads = int(q.shape[1])
+        self.scale = 1.0 / math.sqrt(int(q.shape[2]))
+        self.chunk = chunk
+        self.ws = ctypes.byref(ws.desc)
+        self.s = ctypes.c_void_p(stream.cuda_stream)
+        self.check = _lib.check
+
+    def write(self):
+        self.check(self.lib.pkv_kv_write(self.cref, self.layer, self.k, self.v, self.n_new, self.s),
+                   "pkv_kv_write")
+
+    def decode(self):
+        self.check(self.lib.pkv_paged_decode_chunked(self.cref, self.layer, self.q, self.o,
+                                                     self.heads, self.scale, self.chunk, self.ws,
+                                                     self.s), "pkv_paged_decode")
+
+
+def timed(torch, stream, fn, steps, warmup, flush, parts=None):
+    """Run fn `warmup` times, then `steps` times with an L2 flush before each;
+    CUDA events on `stream` bracket each step (and each part, if given)."""
+    for _ in range(warmup):
+        flush.add_(1)
+        fn()
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(steps):
+        flush.add_(1)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2 + (len(parts) if parts else 0))]
+        e[0].record(stream)
+        if parts:
+            for j, p in enumerate(parts):
+                p()
+                e[1 + j].record(stream)
+        else:
+            fn()
+            e[1].record(stream)
+        ev.append(e)
+    torch.cuda.synchronize()
+    total = [e[0].elapsed_time(e[-1]) for e in ev]
+    per_part = None
+    if parts:
+        per_part = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(len(parts))]
+    return total, per_part
+
+
+def run_pkv(args):
+    import torch
+    import paged_kv_cache_loc_gb300 as pkv
+    from paged_kv_cache_loc_gb300 import _lib, build
+    from paged_kv_cache_loc_gb300 import workloads as W
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    lib = _lib.load()
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # ---- the workload: batched GQA decode -------------------------------
+    case = W.batched_decode(seed=1002 + 100 * rank)
+    cache, q, kn, vn = W.upload(case, dev)
+    o = torch.empty_like(q)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024, device=dev)
+    chunk = args.chunk
+    if chunk == 0:
+        chunk, _ = pkv.decode_plan(cache, case.n_heads, ws)
+    n_splits = -(-case.max_len // chunk)
+    step = DecodeStep(lib, cache, q, kn, vn, o, ws, case.layer_id, chunk, stream)
+    launches_per_step = 1 + 1 + (0 if n_splits == 1 else 1)
+
+    with torch.cuda.stream(stream):
+        if world > 1:
+            torch.distributed.barrier()
+        sampler = ClockSampler(local)
+        sampler.start()
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        step_ms, parts = timed(torch, stream, None, args.steps, args.warmup, flush,
+                               parts=[step.write, step.decode])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
+    st, detail = pkv.last_device_error(stream, dev)
+    if st != 0:
+        raise RuntimeError(f"device error word set during the benchmark (detail {detail})")
+
+    ms_step = statistics.mean(step_ms)
+    ms_write = statistics.mean(parts[0])
+    ms_decode = statistics.mean(parts[1])
+    b_dec = decode_bytes(case)
+    b_wr = kv_write_bytes(case)
+    total_ms = ms_step
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * (b_dec + b_wr) / (total_ms * 1e-3) / 1e9
+
+    achieved = b_dec / (ms_decode * 1e-3) / 1e9
+    roofline = {
+        "bound": "hbm", "kernel": "paged_decode (split + merge)",
+        "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": round(achieved / peaks["hbm_gbs"], 4),
+        "peak_source": peaks["hbm_source"],
+        "traffic": profile_traffic("decode_batched_b32_traffic.txt", "pkv_decode.cu"),
+        "algorithmic_bytes_per_launch": b_dec,
+        "ms_per_launch": round(ms_decode, 5),
+    }
+
+    out = {
+        "metric": "paged-decode attention KV GB/s (decode step: kv_write + paged_decode), batched GQA decode",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V/q, permuted slots)",
+        "config": {"workload": "batched GQA decode", "batch": case.batch, "n_heads": case.n_heads,
+                   "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
+                   "seq_lens": "uniform [512, 4096]", "total_kv_tokens": int(case.seq_lens.sum()),
+                   "pool_slots": case.size, "n_layers": case.n_layers, "layer_id": case.layer_id,
+                   "page_size": 1, "split_chunk": chunk, "n_splits": n_splits,
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "decode_tokens_per_s": round(world * case.batch / (total_ms * 1e-3), 1),
+        "attention_stack_tokens_per_s": round(world * case.batch / (case.n_layers * total_ms * 1e-3), 1),
+        "kv_write_ms": round(ms_write, 5),
+        "roofline": roofline,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+
+    if not args.no_extras:
+        out["e2e"] = e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev)
+        out["long_context_b1"] = long_context_leg(torch, pkv, W, stream, flush, peaks, dev)
+        out["prefill"] = prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev)
+    if rank == 0 and not args.no_extras:
+        out["cpu_baseline"] = cpu_baseline(case, b_dec + b_wr)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D of q, k_new, v_new and the per-step metadata, kv_write +
+    paged_decode, D2H of o, all inside the events."""
+    from paged_kv_cache_loc_gb300 import workloads as W
+    hq = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(case.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    meta = [torch.from_numpy(a).pin_memory() for a in (case.seq_lens, case.req_pool_indices,
+                                                       case.out_cache_loc, case.kv_indptr)]
+    ho = torch.empty(hq.shape, dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (hq, hk, hv))
+    dmeta = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in meta]
+    do = torch.empty(hq.shape, dtype=torch.bfloat16, device=dev)
+    c = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                    req_to_token=cache.req_to_token, req_pool_indices=dmeta[1],
+                    seq_lens=dmeta[0], out_cache_loc=dmeta[2], kv_indptr=dmeta[3],
+                    max_len=case.max_len)
+
+    def step():
+        for h, d in zip([hq, hk, hv] + meta, [dq, dk, dv] + dmeta):
+            d.copy_(h, non_blocking=True)
+        pkv.kv_write(c, case.layer_id, dk, dv, stream=stream)
+        pkv.paged_decode(c, case.layer_id, dq, do, workspace=ws, chunk=chunk, stream=stream)
+        ho.copy_(do, non_blocking=True)
+
+    n = max(20, args.steps // 4)
+    with torch.cuda.stream(stream):
+        ms, _ = timed(torch, stream, step, n, 5, flush)
+    assert torch.equal(ho, do.cpu())
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + meta)
+    d2h = ho.numel() * ho.element_size()
+    b = decode_bytes(case) + kv_write_bytes(case)
+    t = statistics.mean(ms)
+    return {"value": round(b / (t * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(t, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "path": "pinned host -> device copies, public API (ctypes) calls, device -> pinned host"}
+
+
+def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
+    """B=1 decode at 32768 tokens of context (split-K across the SMs)."""
+    case = W.long_decode(32768)
+    cache, q, kn, vn = W.upload(case, dev)
+    pkv.kv_write(cache, case.layer_id, kn, vn)
+    ws = pkv.Workspace(1, case.n_heads, case.head_dim, 1024, device=dev)
+    o = torch.empty_like(q)
+    chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
+    with torch.cuda.stream(stream):
+        ms, _ = timed(torch, stream,
+                      lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
+                                               stream=stream), 100, 10, flush)
+    t = statistics.median(ms)
+    b = decode_bytes(case)
+    gbs = b / (t * 1e-3) / 1e9
+    return {"context": 32768, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
+            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "split_chunk": chunk,
+            "n_splits": n_splits, "algorithmic_bytes": b}
+
+
+def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
+    """Ragged causal prefill: 16 requests, q_len U[128, 2048], prefix U[0, 4096]."""
+    case = W.ragged_prefill()
+    cache, q, kn, vn = W.upload(case, dev)
+    o = torch.empty_like(q)
+
+    def write():
+        pkv.kv_write(cache, case.layer_id, kn, vn, stream=stream)
+
+    def attend():
+        pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o,
+                          stream=stream)
+    with torch.cuda.stream(stream):
+        ms, parts = timed(torch, stream, None, args.prefill_steps, 3, flush, parts=[write, attend])
+    t_attn = statistics.mean(parts[1])
+    t_wr = statistics.mean(parts[0])
+    fl = prefill_flops(case)
+    tf = fl / (t_attn * 1e-3) / 1e12
+    wb = kv_write_bytes(case)
+    return {"workload": "ragged causal prefill", "total_q": int(case.q_lens.sum()),
+            "causal_flops": fl, "ms_prefill": round(t_attn, 4),
+            "tflops": round(tf, 1), "roofline": {
+                "bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["bf16_source"]},
+            "kv_write_ms": round(t_wr, 4), "kv_write_gbs": round(wb / (t_wr * 1e-3) / 1e9, 1),
+            "kv_write_frac_of_hbm": round(wb / (t_wr * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "ms_per_step": round(statistics.mean(ms), 4)}
+
+
+def cpu_baseline(case, step_bytes):
+    """The fp64 oracle (single-threaded C) on the same decode step."""
+    import oracle
+    from paged_kv_cache_loc_gb300 import workloads as W  # noqa: F401
+    # the oracle's write goes to copies of the touched rows only: rebuild a
+    # small pool holding just this layer so the copy stays cheap
+    t0 = time.perf_counter()
+    kb = case.k_buffer[case.layer_id:case.layer_id + 1].copy()
+    vb = case.v_buffer[case.layer_id:case.layer_id + 1].copy()
+    t_copy = time.perf_counter() - t0
+    reps = []
+    for _ in range(2):
+        t0 = time.perf_counter()
+        oracle.kv_write(kb, vb, 0, case.k_new, case.v_new, case.out_cache_loc)
+        oracle.decode(kb, vb, case.req_to_token, case.req_pool_indices, case.seq_lens, case.q, 0)
+        reps.append(time.perf_counter() - t0)
+    t = min(reps)
+    return {"value": round(step_bytes / t / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds_per_step": round(t, 3),
+            "sample": "the full decode step (kv_write of 32 rows + decode of all 32 requests, "
+                      "all heads), best of 2; pool restricted to the target layer "
+                      f"(copy {t_copy:.2f}s, untimed)", "host_threads_available": os.cpu_count()}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_loc_gb300 import workloads as W
+    case = W.batched_decode()
+    kb = case.k_buffer[case.layer_id:case.layer_id + 1].copy()
+    vb = case.v_buffer[case.layer_id:case.layer_id + 1].copy()
+    oracle.kv_write(kb, vb, 0, case.k_new, case.v_new, case.out_cache_loc)
+    # each step: the decode of one request (all heads) and its cache write,
+    # cycling through the batch
+    per_req = []
+    for b in range(case.batch):
+        sub = dict(req_pool_indices=case.req_pool_indices[b:b + 1], seq_lens=case.seq_lens[b:b + 1],
+                   q=case.q[b:b + 1])
+        tok = int(case.seq_lens[b])
+        row = case.n_kv_heads * case.head_dim * 2
+        nbytes = tok * 2 * row + tok * 4 + 2 * case.n_heads * case.head_dim * 2 + (2 * row * 2 + 4)
+        per_req.append((sub, nbytes, b))
+
+    def one(i):
+        sub, nbytes, b = per_req[i % case.batch]
+        oracle.kv_write(kb, vb, 0, case.k_new[b:b + 1], case.v_new[b:b + 1],
+                        case.out_cache_loc[b:b + 1])
+        oracle.decode(kb, vb, case.req_to_token, sub["req_pool_indices"], sub["seq_lens"], sub["q"], 0)
+        return nbytes
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(args.steps):
+        total += one(i)
+    t = time.perf_counter() - t0
+    value = total / t / 1e9
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "paged-decode attention KV GB/s (decode step: kv_write + paged_decode), batched GQA decode",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) K/V/q, permuted slots)",
+        "config": {"workload": "batched GQA decode", "batch": case.batch, "n_heads": case.n_heads,
+                   "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
+                   "seq_lens": "uniform [512, 4096]"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step = one request's cache write + decode (all 32 heads), "
+                                   "cycling through the 32 requests of the workload"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache hot path.
+ *
+ * The operations and names come from AstrAI's inference design
+ * (docs/guides/inference.md):
+ *   - "KV Cache": decode attention o_n = sum_j softmax(q_n k_j / sqrt(d_k)) v_j;
+ *     RoPE is applied before the cache write;
+ *   - "KVCache System": KVStorage k_buffer / v_buffer [n_layers, size,
+ *     n_kv_heads, head_dim]; ReqToTokenPool req_to_token [num_reqs,
+ *     max_ctx_len] (logical position -> physical token slot); the KVCache
+ *     dataclass fields req_pool_indices, seq_lens, out_cache_loc, max_len,
+ *     kv_indptr, qo_indptr; the write k_buffer[layer_id, out_cache_loc] = k;
+ *   - "Attention Backend": decode writes K/V then attends through req_to_token
+ *     with page_size 1; prefill writes K/V then attends over a ragged batch
+ *     addressed by qo_indptr / kv_indptr;
+ *   - "Rotary Embedding Backend": freqs_cis [max_len, dim/2, 2] f32 (cos, sin).
+ * The commit log under tests/inference/test_cache.py fixes int32 page-table,
+ * request-row and cache-location indices, and a workspace allocated once that
+ * owns the split-K partials decode_o_part / decode_ml_part so that CUDA-graph
+ * replay sees stable addresses.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are caller-owned DEVICE memory, row-major and contiguous.
+ *     The library never allocates, frees or copies host<->device.
+ *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Work is enqueued asynchronously; the call returns once enqueued.
+ *   - Return value: PKV_OK or a negative PKV_ERR_* code.  Errors the host can
+ *     see (null pointers, shapes, sizes, alignment, unsupported variants) are
+ *     returned before anything is enqueued.  Errors in device-resident data
+ *     (a slot outside [0, size), a request row outside [0, num_reqs), a length
+ *     beyond max_ctx_len / max_len, kv_len < q_len) never fault: the kernel
+ *     substitutes a safe index, records the first such error in a per-device
+ *     error word and finishes; pkv_last_device_error() reports it.  Results
+ *     of a call that recorded such an error are unspecified.
+ *   - Nothing traps, aborts or waits without a bound.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage element type of k_buffer / v_buffer; q, k, v and o use the same. */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+enum {
+    PKV_OK = 0,
+    PKV_ERR_ARG = -1,         /* bad pointer, shape, size, alignment or index range */
+    PKV_ERR_UNSUPPORTED = -2, /* valid request that this build has no kernel for */
+    PKV_ERR_WORKSPACE = -3,   /* workspace missing, uninitialised or too small */
+    PKV_ERR_INDEX = -4,       /* device data out of range (from pkv_last_device_error) */
+    PKV_ERR_CUDA = -5         /* a CUDA runtime call or launch failed */
+};
+
+/*
+ * The KVCache dataclass of "KVCache System", as plain pointers and sizes.
+ *   k_buffer, v_buffer  [n_layers, size, n_kv_heads, head_dim] of dtype; the
+ *                       row of (layer, slot) is n_kv_heads*head_dim elements.
+ *   req_to_token        int32 [num_reqs, max_ctx_len]: physical slot of each
+ *                       logical position of each request row.  page_size > 1
+ *                       pools are expressed per token (a page is a run of
+ *                       page_size consecutive slots).
+ *   req_pool_indices    int32 [batch]: request row of each batch entry.
+ *   seq_lens            int32 [batch]: decode context length of each entry,
+ *                       INCLUDING the token written this step.
+ *   kv_indptr           int32 [batch + 1]: prefix sums of the kv lengths; in
+ *                       prefill the kv length of entry b is
+ *                       kv_indptr[b+1] - kv_indptr[b] (cached prefix + new
+ *                       tokens).  Decode does not read it (may be NULL).
+ *   qo_indptr           int32 [batch + 1]: prefix sums of the query lengths
+ *                       (prefill only; NULL in decode).
+ *   out_cache_loc       int32 [n_new]: destination slot of each new token, in
+ *                       qo_indptr order (the pages' [batch, seq_len] flattened).
+ *   batch               number of batch entries.
+ *   max_len             host-side upper bound of seq_lens (decode) or of the kv
+ *                       lengths (prefill): the pages pass max(seq_lens) on the
+ *                       host so that no device sync is needed.  Launch grids
+ *                       are sized from it.
+ */
+typedef struct pkv_kvcache {
+    void *k_buffer;
+    void *v_buffer;
+    int32_t dtype;            /* pkv_dtype */
+    int32_t n_layers;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int64_t size;
+    const int32_t *req_to_token;
+    int32_t num_reqs;
+    int32_t max_ctx_len;
+    const int32_t *req_pool_indices;
+    const int32_t *seq_lens;
+    const int32_t *kv_indptr;
+    const int32_t *qo_indptr;
+    const int32_t *out_cache_loc;
+    int32_t batch;
+    int32_t max_len;
+} pkv_kvcache;
+
+/*
+ * Caller-owned workspace for the decode split-K partials (the pages'
+ * decode_o_part / decode_ml_part):
+ *   o_part   float [max_batch, n_heads, max_splits, head_dim]: normalised
+ *            attention output of each split of each (entry, head);
+ *   ml_part  float [max_batch, n_heads, max_splits, 2]: (running max in base-2
+ *            units of the scaled score, softmax denominator) of each split.
+ * Allocate pkv_workspace_bytes(...) bytes of device memory once (256-byte
+ * aligned, e.g. straight from cudaMalloc), describe it with
+ * pkv_workspace_init(), and pass the same descriptor to every call so that
+ * the device addresses stay fixed across CUDA-graph replays.  No call needs
+ * its contents to persist between calls; calls that share a workspace must not
+ * overlap on the GPU.
+ */
+typedef struct pkv_workspace {
+    void *base;
+    size_t bytes;
+    int32_t max_batch;
+    int32_t n_heads;
+    int32_t head_dim;
+    int32_t max_splits;
+    float *o_part;
+    float *ml_part;
+    uint32_t magic;           /* set by pkv_workspace_init */
+} pkv_workspace;
+
+/* Bytes needed for a workspace of these dimensions (0 if any is < 1). */
+size_t pkv_workspace_bytes(int32_t max_batch, int32_t n_heads, int32_t head_dim,
+                           int32_t max_splits);
+
+/* Fill *out to describe `base`.  PKV_ERR_ARG on null / misaligned base or bad
+ * dimensions, PKV_ERR_WORKSPACE if `bytes` is smaller than required. */
+int pkv_workspace_init(void *base, size_t bytes, int32_t max_batch, int32_t n_heads,
+                       int32_t head_dim, int32_t max_splits, pkv_workspace *out);
+
+/*
+ * K/V cache write ("KVCache System": k_buffer[layer_id, out_cache_loc] = k):
+ * for i in [0, n_new): row (layer_id, c->out_cache_loc[i]) of c->k_buffer
+ * (resp. v_buffer) becomes k[i] (resp. v[i]).  k, v: [n_new, n_kv_heads,
+ * head_dim] of c->dtype.  Bit-exact copy.  Requires 16-byte aligned buffers
+ * and a row of n_kv_heads*head_dim elements that is a multiple of 16 bytes.
+ * Duplicate destination slots give an unspecified one of the rows.  n_new = 0
+ * is a no-op.  Reads c->out_cache_loc, c->size, c->n_layers, the buffers and
+ * shape fields only.
+ */
+int pkv_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                 int32_t n_new, void *stream);
+
+/*
+ * Fused rotary embedding + K/V cache write ("KV Cache": RoPE before the
+ * write; "Rotary Embedding Backend": freqs_cis [max_pos, head_dim/2, 2] f32).
+ * Row i of k is rotated pairwise, (k[2e] + i k[2e+1]) * (cos + i sin) with
+ * (cos, sin) = freqs_cis[positions[i], e], rounded once to the storage dtype,
+ * and written like pkv_kv_write; v is copied unchanged.  positions: int32
+ * [n_new] device array (a position outside [0, max_pos) is a device-data
+ * error).  head_dim must be even.
+ */
+int pkv_rope_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                      int32_t n_new, const float *freqs_cis, int32_t max_pos,
+                      const int32_t *positions, void *stream);
+
+/*
+ * Paged decode attention ("KV Cache" formula; "Attention Backend" decode path).
+ * For each entry b < c->batch with request row r = c->req_pool_indices[b] and
+ * context n = c->seq_lens[b], and each query head h < n_heads:
+ *   o[b, h] = sum_{j<n} softmax_j(sm_scale * q[b,h] . K[slot_j, h/G]) V[slot_j, h/G],
+ *   slot_j = c->req_to_token[r, j],  G = n_heads / c->n_kv_heads,
+ * with K/V the rows of layer `layer_id`.  q, o: [batch, n_heads, head_dim] of
+ * c->dtype; o must not alias q.  n = 0 gives o = 0.  Accumulation in fp32,
+ * one rounding to the output dtype.  Long contexts are split into chunks
+ * whose partials go to the workspace and are merged by a second kernel; the
+ * split count is chosen on the host from c->max_len, c->batch and the SM count.
+ * Supported: head_dim 64 or 128, G in {1, 2, 4, 8}.
+ */
+int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                     int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
+
+/*
+ * pkv_paged_decode with an explicit split size: every entry's context is cut
+ * into chunks of `chunk` tokens (a positive multiple of 32; 0 = automatic).
+ * The result is the same up to fp32 rounding for any chunk; the workspace
+ * must hold ceil(c->max_len / chunk) splits.
+ */
+int pkv_paged_decode_chunked(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                             int32_t n_heads, float sm_scale, int32_t chunk,
+                             const pkv_workspace *ws, void *stream);
+
+/*
+ * The split plan pkv_paged_decode would use: *chunk tokens per split and
+ * *n_splits = ceil(c->max_len / *chunk) splits.  Host-only; enqueues nothing.
+ */
+int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *ws,
+                    int32_t *chunk, int32_t *n_splits);
+
+/*
+ * Ragged paged prefill ("Attention Backend" prefill path).  Entry b has
+ * q_len = qo_indptr[b+1] - qo_indptr[b] new tokens (already written to the
+ * cache) at the end of a context of kv_len = kv_indptr[b+1] - kv_indptr[b]
+ * positions, so its cached prefix is P = kv_len - q_len.  Packed query row
+ * p = qo_indptr[b] + i, head h attends over positions j < P + i + 1 when
+ * `causal` (the mask of process_attention_mask: a cached prefix is fully
+ * visible), else j < kv_len, reading slot req_to_token[req_pool_indices[b], j]
+ * of kv head h / G.  q, o: [qo_indptr[batch], n_heads, head_dim] bf16.
+ * max_q_len / max_kv_len: host-side upper bounds of q_len and kv_len (grid
+ * sizing).  `ws` may be NULL.  Supported: bf16, head_dim 128 or 64,
+ * G in {1, 2, 4, 8}.
+ */
+int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                      int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,
+                      float sm_scale, const pkv_workspace *ws, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the calling device's error word.
+ * Returns PKV_OK, PKV_ERR_INDEX (device data out of range since the last
+ * read; *detail, if non-NULL, receives the first offending value) or
+ * PKV_ERR_CUDA.
+ */
+int pkv_last_device_error(void *stream, int64_t *detail);
+
+/* Static, human-readable text for a status code. */
+const char *pkv_status_string(int status);
+
+/* Library version string. */
+const char *pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,357 @@
+// pkv_api.cu -- the C ABI declared in include/pkv.h: host-side argument
+// checks, the decode split plan, workspace bookkeeping, the per-device error
+// word, and dispatch to the kernels.  Nothing here allocates device memory.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_common.cuh"
+#include "pkv_launch.h"
+
+namespace {
+
+// The per-device error word written by the kernels (see pkv_common.cuh).
+__device__ pkv::DevErr g_err;
+
+constexpr uint32_t kWsMagic = 0x706b7731u;   // "pkw1"
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    pkv::DevErr *err = nullptr;
+    int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Device-side address of g_err and the SM count of the current device,
+// looked up once per device with that device current.
+int device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.err) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_err) != cudaSuccess) return PKV_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        d.err = static_cast<pkv::DevErr *>(ptr);
+        d.sms = sms;
+    }
+    *out = d;
+    return PKV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+int map_launch(cudaError_t e) {
+    if (e == cudaSuccess) return PKV_OK;
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    return PKV_ERR_CUDA;
+}
+
+// Checks shared by every entry point that touches the pool.
+int check_pool(const pkv_kvcache *c, int32_t layer_id) {
+    if (!c || !c->k_buffer || !c->v_buffer) return PKV_ERR_ARG;
+    if (c->dtype != PKV_F32 && c->dtype != PKV_BF16) return PKV_ERR_ARG;
+    if (c->n_layers <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->size <= 0)
+        return PKV_ERR_ARG;
+    if (c->size > INT32_MAX) return PKV_ERR_ARG;   // slots are int32
+    if (layer_id < 0 || layer_id >= c->n_layers) return PKV_ERR_ARG;
+    if (!aligned16(c->k_buffer) || !aligned16(c->v_buffer)) return PKV_ERR_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(c->n_kv_heads) * c->head_dim * elem_bytes(c->dtype);
+    if (row_bytes % 16) return PKV_ERR_ARG;
+    return PKV_OK;
+}
+
+// Checks for the attention entry points (req_to_token indirection).
+int check_attn(const pkv_kvcache *c, int32_t n_heads, const void *q, const void *o) {
+    if (!c->req_to_token || !c->req_pool_indices) return PKV_ERR_ARG;
+    if (c->num_reqs <= 0 || c->max_ctx_len <= 0 || c->batch < 0 || c->max_len < 0) return PKV_ERR_ARG;
+    if (c->max_len > c->max_ctx_len) return PKV_ERR_ARG;
+    if (n_heads <= 0 || n_heads % c->n_kv_heads) return PKV_ERR_ARG;
+    if (c->batch > 0 && (!q || !o || !aligned16(q) || !aligned16(o))) return PKV_ERR_ARG;
+    if (c->batch > 65535) return PKV_ERR_ARG;   // grid z
+    return PKV_OK;
+}
+
+int ws_check(const pkv_workspace *ws) {
+    if (!ws || ws->magic != kWsMagic || !ws->base) return PKV_ERR_WORKSPACE;
+    return PKV_OK;
+}
+
+// Split plan: about four CTAs per SM of (entry, kv head, split) work if every
+// context were max_len long, chunks of 64..2048 tokens in steps of 32, and
+// never more splits than the workspace holds.
+int plan(const pkv_kvcache *c, int sms, const pkv_workspace *ws, int32_t *chunk_out) {
+    const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
+    const int64_t units = static_cast<int64_t>(c->batch > 0 ? c->batch : 1) * c->n_kv_heads;
+    const int64_t target = static_cast<int64_t>(sms > 0 ? sms : 1) * 4;
+    int64_t chunk = (max_len * units + target - 1) / target;
+    chunk = (chunk + 31) / 32 * 32;
+    if (chunk < 64) chunk = 64;
+    if (chunk > pkv::kDecodeMaxChunk) chunk = pkv::kDecodeMaxChunk;
+    int64_t cap_splits = pkv::kDecodeMaxSplits;
+    if (ws_check(ws) == PKV_OK) {
+        if (ws->max_splits < cap_splits) cap_splits = ws->max_splits;
+    } else {
+        cap_splits = 1;   // no workspace: one split per entry
+    }
+    if ((max_len + chunk - 1) / chunk > cap_splits) {
+        chunk = (max_len + cap_splits - 1) / cap_splits;
+        chunk = (chunk + 31) / 32 * 32;
+    }
+    if (chunk > pkv::kDecodeMaxChunk) return PKV_ERR_WORKSPACE;
+    *chunk_out = static_cast<int32_t>(chunk);
+    return PKV_OK;
+}
+
+int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, int32_t n_heads,
+                float sm_scale, int32_t chunk, const pkv_workspace *ws, void *stream) {
+    int rc = check_pool(c, layer_id);
+    if (rc) return rc;
+    rc = check_attn(c, n_heads, q, o);
+    if (rc) return rc;
+    if (!c->seq_lens) return PKV_ERR_ARG;
+    if (!isfinite(sm_scale)) return PKV_ERR_ARG;
+    const int group = n_heads / c->n_kv_heads;
+    if (!pkv::decode_supported(c->dtype, c->head_dim, group)) return PKV_ERR_UNSUPPORTED;
+    if (c->batch == 0) return PKV_OK;
+    if (q == o) return PKV_ERR_ARG;
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc) return rc;
+    if (chunk == 0) {
+        rc = plan(c, di.sms, ws, &chunk);
+        if (rc) return rc;
+    }
+    if (chunk <= 0 || chunk % 32 || chunk > pkv::kDecodeMaxChunk) return PKV_ERR_ARG;
+    const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
+    const int64_t n_splits = (max_len + chunk - 1) / chunk;
+    if (n_splits > pkv::kDecodeMaxSplits) return PKV_ERR_ARG;
+
+    pkv::DecodeParams p{};
+    p.direct = n_splits == 1;
+    if (!p.direct) {
+        rc = ws_check(ws);
+        if (rc) return rc;
+        const int64_t need_o = static_cast<int64_t>(c->batch) * n_heads * n_splits * c->head_dim;
+        const int64_t cap_o = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits *
+                              ws->head_dim;
+        const int64_t need_ml = static_cast<int64_t>(c->batch) * n_heads * n_splits * 2;
+        const int64_t cap_ml = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * 2;
+        if (need_o > cap_o || need_ml > cap_ml) return PKV_ERR_WORKSPACE;
+        p.o_part = ws->o_part;
+        p.ml_part = ws->ml_part;
+    }
+    p.q = q;
+    p.o = o;
+    p.k_buffer = c->k_buffer;
+    p.v_buffer = c->v_buffer;
+    p.req_to_token = c->req_to_token;
+    p.req_pool_indices = c->req_pool_indices;
+    p.seq_lens = c->seq_lens;
+    p.size = c->size;
+    p.layer_row0 = static_cast<int64_t>(layer_id) * c->size;
+    p.n_kv_heads = c->n_kv_heads;
+    p.n_heads = n_heads;
+    p.num_reqs = c->num_reqs;
+    p.max_ctx_len = c->max_ctx_len;
+    p.batch = c->batch;
+    p.max_len = c->max_len;
+    p.chunk = chunk;
+    p.n_splits = static_cast<int32_t>(n_splits);
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.err = di.err;
+    return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, group,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int kv_write_impl(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                  int32_t n_new, const float *freqs_cis, int32_t max_pos,
+                  const int32_t *positions, bool rope, void *stream) {
+    int rc = check_pool(c, layer_id);
+    if (rc) return rc;
+    if (n_new < 0) return PKV_ERR_ARG;
+    if (n_new == 0) return PKV_OK;
+    if (!k || !v || !c->out_cache_loc || !aligned16(k) || !aligned16(v)) return PKV_ERR_ARG;
+    const int64_t row_chunks =
+        static_cast<int64_t>(c->n_kv_heads) * c->head_dim * elem_bytes(c->dtype) / 16;
+    if (2 * static_cast<int64_t>(n_new) * row_chunks >= INT32_MAX) return PKV_ERR_ARG;
+    if (rope) {
+        if (!freqs_cis || !positions || max_pos <= 0 || !aligned16(freqs_cis)) return PKV_ERR_ARG;
+        if ((c->head_dim * elem_bytes(c->dtype)) % 16) return PKV_ERR_ARG;   // chunks stay in a head
+    }
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc) return rc;
+    pkv::KvWriteParams p{};
+    p.k = k;
+    p.v = v;
+    p.k_buffer = c->k_buffer;
+    p.v_buffer = c->v_buffer;
+    p.out_cache_loc = c->out_cache_loc;
+    p.n_new = n_new;
+    p.size = c->size;
+    p.layer_row0 = static_cast<int64_t>(layer_id) * c->size;
+    p.row_chunks = static_cast<int32_t>(row_chunks);
+    p.head_dim = c->head_dim;
+    p.dtype = c->dtype;
+    p.freqs_cis = freqs_cis;
+    p.positions = positions;
+    p.max_pos = max_pos;
+    p.err = di.err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return map_launch(rope ? pkv::launch_rope_kv_write(p, s) : pkv::launch_kv_write(p, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_workspace_bytes(int32_t max_batch, int32_t n_heads, int32_t head_dim,
+                           int32_t max_splits) {
+    if (max_batch < 1 || n_heads < 1 || head_dim < 1 || max_splits < 1) return 0;
+    const size_t units = static_cast<size_t>(max_batch) * n_heads * max_splits;
+    const size_t o_bytes = (units * head_dim * sizeof(float) + 255) / 256 * 256;
+    return o_bytes + units * 2 * sizeof(float);
+}
+
+int pkv_workspace_init(void *base, size_t bytes, int32_t max_batch, int32_t n_heads,
+                       int32_t head_dim, int32_t max_splits, pkv_workspace *out) {
+    if (!out || !base || (reinterpret_cast<uintptr_t>(base) & 255u)) return PKV_ERR_ARG;
+    const size_t need = pkv_workspace_bytes(max_batch, n_heads, head_dim, max_splits);
+    if (need == 0) return PKV_ERR_ARG;
+    if (bytes < need) return PKV_ERR_WORKSPACE;
+    const size_t units = static_cast<size_t>(max_batch) * n_heads * max_splits;
+    const size_t o_bytes = (units * head_dim * sizeof(float) + 255) / 256 * 256;
+    out->base = base;
+    out->bytes = bytes;
+    out->max_batch = max_batch;
+    out->n_heads = n_heads;
+    out->head_dim = head_dim;
+    out->max_splits = max_splits;
+    out->o_part = static_cast<float *>(base);
+    out->ml_part = reinterpret_cast<float *>(static_cast<char *>(base) + o_bytes);
+    out->magic = kWsMagic;
+    return PKV_OK;
+}
+
+int pkv_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                 int32_t n_new, void *stream) {
+    return kv_write_impl(c, layer_id, k, v, n_new, nullptr, 0, nullptr, false, stream);
+}
+
+int pkv_rope_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                      int32_t n_new, const float *freqs_cis, int32_t max_pos,
+                      const int32_t *positions, void *stream) {
+    return kv_write_impl(c, layer_id, k, v, n_new, freqs_cis, max_pos, positions, true, stream);
+}
+
+int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                     int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream) {
+    return decode_impl(c, layer_id, q, o, n_heads, sm_scale, 0, ws, stream);
+}
+
+int pkv_paged_decode_chunked(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                             int32_t n_heads, float sm_scale, int32_t chunk,
+                             const pkv_workspace *ws, void *stream) {
+    if (chunk < 0) return PKV_ERR_ARG;
+    return decode_impl(c, layer_id, q, o, n_heads, sm_scale, chunk, ws, stream);
+}
+
+int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *ws,
+                    int32_t *chunk, int32_t *n_splits) {
+    if (!c || !chunk || !n_splits || c->n_kv_heads <= 0 || n_heads <= 0 || c->max_len < 0)
+        return PKV_ERR_ARG;
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    rc = plan(c, di.sms, ws, chunk);
+    if (rc) return rc;
+    const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
+    *n_splits = static_cast<int32_t>((max_len + *chunk - 1) / *chunk);
+    return PKV_OK;
+}
+
+int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                      int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,
+                      float sm_scale, const pkv_workspace *ws, void *stream) {
+    (void)ws;
+    int rc = check_pool(c, layer_id);
+    if (rc) return rc;
+    rc = check_attn(c, n_heads, q, o);
+    if (rc) return rc;
+    if (!c->qo_indptr || !c->kv_indptr) return PKV_ERR_ARG;
+    if (max_q_len < 0 || max_kv_len < 0 || max_q_len > max_kv_len || max_kv_len > c->max_ctx_len)
+        return PKV_ERR_ARG;
+    if (!isfinite(sm_scale)) return PKV_ERR_ARG;
+    const int group = n_heads / c->n_kv_heads;
+    if (!pkv::prefill_supported(c->dtype, c->head_dim, group)) return PKV_ERR_UNSUPPORTED;
+    if (c->batch == 0 || max_q_len == 0) return PKV_OK;
+    if (q == o) return PKV_ERR_ARG;
+    if (static_cast<int64_t>(max_q_len) * group / 64 + 1 > INT32_MAX) return PKV_ERR_ARG;
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc) return rc;
+    pkv::PrefillParams p{};
+    p.q = q;
+    p.o = o;
+    p.k_buffer = c->k_buffer;
+    p.v_buffer = c->v_buffer;
+    p.req_to_token = c->req_to_token;
+    p.req_pool_indices = c->req_pool_indices;
+    p.qo_indptr = c->qo_indptr;
+    p.kv_indptr = c->kv_indptr;
+    p.size = c->size;
+    p.layer_row0 = static_cast<int64_t>(layer_id) * c->size;
+    p.n_kv_heads = c->n_kv_heads;
+    p.n_heads = n_heads;
+    p.num_reqs = c->num_reqs;
+    p.max_ctx_len = c->max_ctx_len;
+    p.batch = c->batch;
+    p.causal = causal ? 1 : 0;
+    p.max_q_len = max_q_len;
+    p.max_kv_len = max_kv_len;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.err = di.err;
+    return map_launch(pkv::launch_prefill(p, c->dtype, c->head_dim, group,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_last_device_error(void *stream, int64_t *detail) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    pkv::DevErr host{};
+    if (cudaMemcpy(&host, di.err, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (!host.flag) return PKV_OK;
+    if (detail) *detail = host.detail;
+    if (cudaMemset(di.err, 0, sizeof host) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_ERR_INDEX;
+}
+
+const char *pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported variant (dtype, head_dim or group size)";
+        case PKV_ERR_WORKSPACE: return "workspace missing, uninitialised or too small";
+        case PKV_ERR_INDEX: return "device data out of range (slot, request row or length)";
+        case PKV_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+const char *pkv_version(void) { return "pkv 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// pkv_kv_write.cu -- K/V cache write k_buffer[layer_id, out_cache_loc] = k
+// (AstrAI docs/guides/inference.md, "KVCache System"), and the same write with
+// the rotary embedding applied to K first ("KV Cache": RoPE before the write;
+// "Rotary Embedding Backend": freqs_cis [max_len, dim/2, 2] cos/sin pairs).
+//
+// The write is a pure HBM copy: every (token, 16-byte chunk) of the new K and
+// V rows is one work item, consecutive threads take consecutive chunks of a
+// row, so both the reads of k/v and the scattered row writes are fully
+// coalesced 16-byte accesses.  Each thread issues all of its loads before its
+// stores to keep several requests in flight.
+#include "pkv_common.cuh"
+#include "pkv_launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams p) {
+    const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
+    const int32_t total = 2 * per_buf;
+    const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
+    uint4 val[kUnroll];
+    uint4 *dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int32_t idx = base + u * kThreads;
+        dst[u] = nullptr;
+        if (idx < total) {
+            const bool is_v = idx >= per_buf;
+            const int32_t rem = is_v ? idx - per_buf : idx;
+            const int32_t i = rem / p.row_chunks;
+            const int32_t c = rem - i * p.row_chunks;
+            long long loc = __ldg(p.out_cache_loc + i);
+            if (static_cast<unsigned long long>(loc) >= static_cast<unsigned long long>(p.size)) {
+                record_error(p.err, loc);
+                continue;
+            }
+            const uint4 *src = static_cast<const uint4 *>(is_v ? p.v : p.k) + rem;
+            val[u] = __ldg(src);
+            uint4 *buf = static_cast<uint4 *>(is_v ? p.v_buffer : p.k_buffer);
+            dst[u] = buf + (p.layer_row0 + loc) * p.row_chunks + c;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+        if (dst[u]) *dst[u] = val[u];
+}
+
+// Rotate the pairs of one 16-byte chunk of a K row.  `pair0` is the index of
+// the chunk's first (even, odd) pair within its head; cs points at
+// freqs_cis[pos, pair0, 0].
+__device__ __forceinline__ uint4 rotate_chunk_bf16(uint4 x, const float *cs) {
+    const float4 c0 = *reinterpret_cast<const float4 *>(cs);      // pairs 0,1
+    const float4 c1 = *reinterpret_cast<const float4 *>(cs + 4);  // pairs 2,3
+    const float cosv[4] = {c0.x, c0.z, c1.x, c1.z};
+    const float sinv[4] = {c0.y, c0.w, c1.y, c1.w};
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float re = bf16lo(w[j]), im = bf16hi(w[j]);
+        const float ore = re * cosv[j] - im * sinv[j];
+        const float oim = re * sinv[j] + im * cosv[j];
+        const __nv_bfloat162 r = __floats2bfloat162_rn(ore, oim);
+        w[j] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint4 rotate_chunk_f32(uint4 x, const float *cs) {
+    const float4 c = *reinterpret_cast<const float4 *>(cs);   // pairs 0,1
+    const float re0 = __uint_as_float(x.x), im0 = __uint_as_float(x.y);
+    const float re1 = __uint_as_float(x.z), im1 = __uint_as_float(x.w);
+    return make_uint4(__float_as_uint(re0 * c.x - im0 * c.y), __float_as_uint(re0 * c.y + im0 * c.x),
+                      __float_as_uint(re1 * c.z - im1 * c.w), __float_as_uint(re1 * c.w + im1 * c.z));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) rope_kv_write_kernel(const KvWriteParams p) {
+    constexpr int kElemsPerChunk = BF16 ? 8 : 4;
+    const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
+    const int32_t total = 2 * per_buf;
+    const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
+    const int chunks_per_head = p.head_dim / kElemsPerChunk;
+    uint4 val[kUnroll];
+    uint4 *dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int32_t idx = base + u * kThreads;
+        dst[u] = nullptr;
+        if (idx < total) {
+            const bool is_v = idx >= per_buf;
+            const int32_t rem = is_v ? idx - per_buf : idx;
+            const int32_t i = rem / p.row_chunks;
+            const int32_t c = rem - i * p.row_chunks;
+            long long loc = __ldg(p.out_cache_loc + i);
+            if (static_cast<unsigned long long>(loc) >= static_cast<unsigned long long>(p.size)) {
+                record_error(p.err, loc);
+                continue;
+            }
+            uint4 x = __ldg(static_cast<const uint4 *>(is_v ? p.v : p.k) + rem);
+            if (!is_v) {
+                const int pos = __ldg(p.positions + i);
+                if (static_cast<unsigned>(pos) >= static_cast<unsigned>(p.max_pos)) {
+                    record_error(p.err, pos);
+                    continue;
+                }
+                const int pair0 = (c % chunks_per_head) * (kElemsPerChunk / 2);
+                const float *cs = p.freqs_cis + (static_cast<int64_t>(pos) * (p.head_dim / 2) + pair0) * 2;
+                x = BF16 ? rotate_chunk_bf16(x, cs) : rotate_chunk_f32(x, cs);
+            }
+            val[u] = x;
+            uint4 *buf = static_cast<uint4 *>(is_v ? p.v_buffer : p.k_buffer);
+            dst[u] = buf + (p.layer_row0 + loc) * p.row_chunks + c;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+        if (dst[u]) *dst[u] = val[u];
+}
+
+inline unsigned grid_for(const KvWriteParams &p) {
+    const long long total = 2LL * p.n_new * p.row_chunks;
+    return static_cast<unsigned>((total + kThreads * kUnroll - 1) / (kThreads * kUnroll));
+}
+
+}  // namespace
+
+cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s) {
+    if (p.n_new == 0) return cudaSuccess;
+    kv_write_kernel<<<grid_for(p), kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_kv_write(const KvWriteParams &p, cudaStream_t s) {
+    if (p.n_new == 0) return cudaSuccess;
+    if (p.dtype == PKV_BF16)
+        rope_kv_write_kernel<true><<<grid_for(p), kThreads, 0, s>>>(p);
+    else
+        rope_kv_write_kernel<false><<<grid_for(p), kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,95 @@
+// pkv_launch.h -- internal launch interfaces between the C ABI (pkv_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct DevErr;
+
+// K/V cache write (optionally with the rotary embedding applied to K).
+struct KvWriteParams {
+    const void *k;              // [n_new, n_kv_heads, head_dim]
+    const void *v;
+    void *k_buffer;             // pool base
+    void *v_buffer;
+    const int32_t *out_cache_loc;
+    int64_t n_new;
+    int64_t size;               // slots per layer
+    int64_t layer_row0;         // layer_id * size
+    int32_t row_chunks;         // 16-byte chunks per (layer, slot) row
+    int32_t head_dim;
+    int32_t dtype;              // pkv_dtype
+    const float *freqs_cis;     // rope only: [max_pos, head_dim/2, 2]
+    const int32_t *positions;   // rope only: [n_new]
+    int32_t max_pos;
+    DevErr *err;
+};
+
+// Split-K paged decode.
+struct DecodeParams {
+    const void *q;              // [batch, n_heads, head_dim]
+    void *o;                    // [batch, n_heads, head_dim]
+    const void *k_buffer;
+    const void *v_buffer;
+    const int32_t *req_to_token;
+    const int32_t *req_pool_indices;
+    const int32_t *seq_lens;
+    float *o_part;              // [batch, n_heads, n_splits, head_dim]
+    float *ml_part;             // [batch, n_heads, n_splits, 2]
+    int64_t size;
+    int64_t layer_row0;
+    int32_t n_kv_heads;
+    int32_t n_heads;
+    int32_t num_reqs;
+    int32_t max_ctx_len;
+    int32_t batch;
+    int32_t max_len;
+    int32_t chunk;              // tokens per split (multiple of 32)
+    int32_t n_splits;           // ceil(max_len / chunk)
+    int32_t direct;             // 1: single split, write o directly (no merge)
+    float scale_log2;           // sm_scale * log2(e)
+    DevErr *err;
+};
+
+// Ragged causal prefill.
+struct PrefillParams {
+    const void *q;              // [total_q, n_heads, head_dim]
+    void *o;
+    const void *k_buffer;
+    const void *v_buffer;
+    const int32_t *req_to_token;
+    const int32_t *req_pool_indices;
+    const int32_t *qo_indptr;
+    const int32_t *kv_indptr;
+    int64_t size;
+    int64_t layer_row0;
+    int32_t n_kv_heads;
+    int32_t n_heads;
+    int32_t num_reqs;
+    int32_t max_ctx_len;
+    int32_t batch;
+    int32_t causal;
+    int32_t max_q_len;
+    int32_t max_kv_len;
+    float scale_log2;
+    DevErr *err;
+};
+
+constexpr int kDecodeMaxChunk = 2048;   // slot indices staged per split
+constexpr int kDecodeMaxSplits = 1024;  // merge kernel limit
+
+// Each returns cudaSuccess or the launch error.  Unsupported variants return
+// cudaErrorNotSupported and enqueue nothing.
+cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s);
+cudaError_t launch_rope_kv_write(const KvWriteParams &p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, int group,
+                          cudaStream_t s);
+bool decode_supported(int dtype, int head_dim, int group);
+cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group,
+                           cudaStream_t s);
+bool prefill_supported(int dtype, int head_dim, int group);
+
+}  // namespace pkv

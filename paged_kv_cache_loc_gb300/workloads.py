@@ -286,3 +286,31 @@ def prefill_sample_rows(case: Case, n_random: int = 64, seed: int = 7) -> np.nda
         picks.update(int(x) for x in rng.integers(0, ql, size=min(n_random, ql)))
         out.extend(lo + p for p in sorted(picks))
     return np.asarray(out, np.int64)
+
+
+def upload(case: Case, device="cuda"):
+    """Copy a case to the device: returns (KVCache, q, k_new, v_new) torch tensors.
+
+    The pool is copied as-is (pre-write); callers run the write themselves."""
+    from .ops import KVCache   # torch-only plumbing, no arithmetic
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+
+    cache = KVCache(k_buffer=dev(case.k_buffer), v_buffer=dev(case.v_buffer),
+                    req_to_token=dev(case.req_to_token),
+                    req_pool_indices=dev(case.req_pool_indices), seq_lens=dev(case.seq_lens),
+                    out_cache_loc=dev(case.out_cache_loc), max_len=case.max_len,
+                    kv_indptr=dev(case.kv_indptr), qo_indptr=dev(case.qo_indptr))
+    return cache, dev(case.q), dev(case.k_new), dev(case.v_new)
+
+
+def host_of(t) -> np.ndarray:
+    """Device tensor -> numpy (bf16 as uint16 bits, others as is)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()

@@ -1,0 +1,340 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Pass bars: kv_write bit-exact over the whole pool; fp32 storage max |err| <=
+1e-5; bf16 storage (fp32 accumulation) max |err| <= 2e-2 and mean |err| <= 2e-3.
+Inputs are the seeded synthetic workloads of paged_kv_cache_loc_gb300.workloads.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_loc_gb300 as pkv
+from paged_kv_cache_loc_gb300 import _lib, build
+from paged_kv_cache_loc_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32_MAX = 1e-5
+TOL_BF16_MAX = 2e-2
+TOL_BF16_MEAN = 2e-3
+
+
+@pytest.fixture(scope="session", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _lib.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def f64(t):
+    return oracle.to_f64(W.host_of(t))
+
+
+def assert_close(got, ref, dtype, what=""):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    if dtype == "f32":
+        assert err.max() <= TOL_F32_MAX, f"{what}: max err {err.max():.3g}"
+    else:
+        assert err.max() <= TOL_BF16_MAX, f"{what}: max err {err.max():.3g}"
+        assert err.mean() <= TOL_BF16_MEAN, f"{what}: mean err {err.mean():.3g}"
+
+
+def no_device_error():
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_OK, f"device error word set (detail {detail})"
+
+
+def prepare(case):
+    """Upload the pre-write pool, write the new rows on the GPU, and apply the
+    oracle's write to the host copy (which then holds the expected pool)."""
+    cache, q, kn, vn = W.upload(case)
+    pkv.kv_write(cache, case.layer_id, kn, vn)
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    return cache, q
+
+
+def ws_for(case, splits=1024):
+    return pkv.Workspace(max(case.batch, 1), case.n_heads, case.head_dim, splits)
+
+
+def oracle_decode(case, **kw):
+    return oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.seq_lens, case.q, case.layer_id, kv_indptr=case.kv_indptr, **kw)
+
+
+def check_pool_bit_exact(cache, case):
+    assert np.array_equal(W.host_of(cache.k_buffer), case.k_buffer)
+    assert np.array_equal(W.host_of(cache.v_buffer), case.v_buffer)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_decode_fp32_all_split_sizes():
+    case = W.tiny_decode()
+    cache, q = prepare(case)
+    check_pool_bit_exact(cache, case)
+    ref = oracle_decode(case)
+    ws = ws_for(case)
+    outs = {}
+    for chunk in (0, 32, 64, 96, 256):
+        o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws, chunk=chunk)
+        no_device_error()
+        outs[chunk] = f64(o)
+        assert_close(outs[chunk], ref, "f32", f"chunk {chunk}")
+    # split count changes only the fp32 summation order
+    for chunk, o in outs.items():
+        assert np.abs(o - outs[256]).max() <= 1e-6
+
+
+@pytest.fixture(scope="module")
+def batched():
+    case = W.batched_decode()
+    cache, q = prepare(case)
+    return case, cache, q
+
+
+def test_batched_decode_kv_write_bit_exact(batched):
+    case, cache, _ = batched
+    check_pool_bit_exact(cache, case)
+
+
+def test_batched_decode_full(batched):
+    case, cache, q = batched
+    ws = ws_for(case)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "batched decode")
+
+
+@pytest.mark.parametrize("chunk", [32, 512, 2048])
+def test_batched_decode_split_invariance(batched, chunk):
+    case, cache, q = batched
+    ws = ws_for(case)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws, chunk=chunk)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", f"chunk {chunk}")
+
+
+@pytest.mark.parametrize("ctx", W.LONG_CONTEXTS)
+def test_long_context_decode(ctx):
+    case = W.long_decode(ctx)
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", f"ctx {ctx}")
+
+
+def test_prefix_shared_decode():
+    case = W.prefix_shared_decode()
+    cache, q = prepare(case)
+    check_pool_bit_exact(cache, case)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws_for(case))
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "prefix-shared")
+
+
+def run_prefill(case, causal=True):
+    cache, q = prepare(case)
+    o = pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, causal=causal)
+    no_device_error()
+    return cache, q, o
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_prefill_reduced_full_check(causal):
+    case = W.ragged_prefill(batch=4, q_lo=1, q_hi=256, p_hi=512, size=8192, seed=2005)
+    _, _, o = run_prefill(case, causal)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id, causal=causal)
+    assert_close(f64(o), ref, "bf16", "reduced prefill")
+
+
+def test_ragged_prefill_full_size_sampled():
+    case = W.ragged_prefill()
+    cache, q, o = run_prefill(case)
+    check_pool_bit_exact(cache, case)
+    rows = W.prefill_sample_rows(case, n_random=16)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id, rows=rows)
+    assert_close(f64(o)[rows], ref, "bf16", "full prefill (sampled rows)")
+
+
+# ---------------------------------------------------------------------------
+# edge cases and variants
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,heads,hk,d", [
+    ("bf16", 8, 8, 128), ("bf16", 16, 8, 128), ("bf16", 32, 4, 128), ("bf16", 16, 4, 64),
+    ("f32", 32, 8, 128), ("f32", 8, 1, 64), ("f32", 4, 2, 64),
+])
+def test_decode_variants_and_ragged_lengths(dtype, heads, hk, d):
+    kv = [0, 1, 31, 32, 33, 95, 300, 1000]
+    case = W.make_case("edge", mode="decode", dtype=dtype, n_layers=3, layer_id=2, size=4096,
+                       n_heads=heads, n_kv_heads=hk, head_dim=d, kv_lens=kv,
+                       q_lens=[0 if n == 0 else 1 for n in kv], seed=77, num_reqs=11,
+                       max_ctx_len=1000)
+    # the empty context writes no token, but decode still has a query row for it
+    extra = W._values(np.random.Generator(np.random.PCG64(5)), (1, heads, d), dtype)
+    case.q = np.concatenate([extra, case.q])
+    cache, qd = prepare(case)
+    ref = oracle_decode(case)
+    for chunk in (0, 32, 128, 1024):
+        o = pkv.paged_decode(cache, case.layer_id, qd, workspace=ws_for(case), chunk=chunk)
+        no_device_error()
+        got = f64(o)
+        assert np.all(got[0] == 0.0), "empty context must give 0"
+        assert_close(got, ref, dtype, f"chunk {chunk}")
+
+
+@pytest.mark.parametrize("heads,hk,d", [(8, 8, 128), (16, 8, 128), (64, 8, 128), (32, 8, 64)])
+def test_prefill_variants(heads, hk, d):
+    q_lens = [0, 1, 5, 64, 65, 130]
+    pre = [7, 0, 100, 0, 63, 1]
+    kv = [a + b for a, b in zip(q_lens, pre)]
+    case = W.make_case("pre_edge", mode="prefill", dtype="bf16", n_layers=2, layer_id=1,
+                       size=4096, n_heads=heads, n_kv_heads=hk, head_dim=d, kv_lens=kv,
+                       q_lens=q_lens, seed=88)
+    _, _, o = run_prefill(case)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id)
+    assert_close(f64(o), ref, "bf16", "prefill variants")
+
+
+def test_causal_prefill_row_matches_decode_kernel():
+    """Prefill row i (prefix P) and decode at context P+i+1 agree on the GPU."""
+    case = W.make_case("cross", mode="prefill", dtype="bf16", n_layers=2, layer_id=0, size=2048,
+                       n_heads=32, n_kv_heads=8, head_dim=128, kv_lens=[300], q_lens=[100],
+                       seed=99)
+    cache, q, o = run_prefill(case)
+    P = 200
+    rows = [0, 37, 99]
+    for i in rows:
+        dc = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                         req_to_token=cache.req_to_token, req_pool_indices=cache.req_pool_indices,
+                         seq_lens=torch.tensor([P + i + 1], dtype=torch.int32, device="cuda"),
+                         max_len=P + i + 1)
+        od = pkv.paged_decode(dc, 0, q[i:i + 1].contiguous(), workspace=ws_for(case), chunk=64)
+        assert_close(f64(od)[0], f64(o)[i], "bf16", f"row {i}")
+
+
+def test_rope_kv_write():
+    case = W.make_case("rope", mode="prefill", dtype="bf16", n_layers=2, layer_id=1, size=1024,
+                       n_heads=8, n_kv_heads=4, head_dim=128, kv_lens=[40, 90], q_lens=[40, 60],
+                       seed=123)
+    rng = np.random.Generator(np.random.PCG64(5))
+    max_pos = 256
+    ang = rng.uniform(-math.pi, math.pi, (max_pos, 64)).astype(np.float32)
+    fc = np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32)
+    pos = rng.integers(0, max_pos, case.out_cache_loc.size).astype(np.int32)
+    cache, q, kn, vn = W.upload(case)
+    pkv.rope_kv_write(cache, 1, kn, vn, torch.from_numpy(fc).cuda(), torch.from_numpy(pos).cuda())
+    no_device_error()
+    k_rot = oracle.rope(case.k_new, fc, pos)
+    got_k = f64(cache.k_buffer)[1, case.out_cache_loc]
+    # one bf16 rounding of an fp32 rotation: |err| <= 2^-8 |x| + tiny
+    assert np.all(np.abs(got_k - k_rot) <= np.abs(k_rot) * 2.0 ** -8 + 1e-6)
+    assert np.array_equal(W.host_of(cache.v_buffer)[1, case.out_cache_loc], case.v_new)
+
+
+def test_kv_write_duplicate_free_scatter_leaves_other_rows():
+    case = W.make_case("kvw", mode="prefill", dtype="f32", n_layers=3, layer_id=0, size=3000,
+                       n_heads=4, n_kv_heads=2, head_dim=64, kv_lens=[700, 5, 1200],
+                       q_lens=[700, 5, 600], seed=9)
+    cache, _ = prepare(case)
+    no_device_error()
+    check_pool_bit_exact(cache, case)
+
+
+def test_device_data_errors_are_reported_not_faulted():
+    case = W.make_case("bad", mode="decode", dtype="bf16", n_layers=2, layer_id=1, size=512,
+                       n_heads=8, n_kv_heads=2, head_dim=128, kv_lens=[20, 40], seed=3)
+    cache, q = prepare(case)
+    no_device_error()
+    ws = ws_for(case)
+    # a slot outside the pool in req_to_token
+    r2t = case.req_to_token.copy()
+    r2t[case.req_pool_indices[1], 7] = case.size + 5
+    bad = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                      req_to_token=torch.from_numpy(r2t).cuda(),
+                      req_pool_indices=cache.req_pool_indices, seq_lens=cache.seq_lens,
+                      max_len=case.max_len)
+    pkv.paged_decode(bad, 1, q, workspace=ws)
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX and detail == case.size + 5
+    # a request row outside req_to_token
+    bad.req_to_token = cache.req_to_token
+    bad.req_pool_indices = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
+    pkv.paged_decode(bad, 1, q, workspace=ws)
+    assert pkv.last_device_error()[0] == _lib.PKV_ERR_INDEX
+    # a write location outside the pool
+    wr = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                     req_to_token=cache.req_to_token, req_pool_indices=cache.req_pool_indices,
+                     out_cache_loc=torch.tensor([3, -1], dtype=torch.int32, device="cuda"))
+    k2 = torch.zeros(2, 2, 128, dtype=torch.bfloat16, device="cuda")
+    pkv.kv_write(wr, 1, k2, k2)
+    assert pkv.last_device_error() == (_lib.PKV_ERR_INDEX, -1)
+    # the context is still healthy and the word was cleared
+    o = pkv.paged_decode(cache, 1, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "after errors")
+
+
+def test_workspace_too_small_is_rejected():
+    case = W.make_case("ws", mode="decode", dtype="bf16", n_layers=1, layer_id=0, size=4096,
+                       n_heads=8, n_kv_heads=2, head_dim=128, kv_lens=[3000], seed=4)
+    cache, q = prepare(case)
+    small = pkv.Workspace(1, 8, 128, 2)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode(cache, 0, q, workspace=small, chunk=32)
+    assert e.value.status == _lib.PKV_ERR_WORKSPACE
+    # the automatic plan respects the workspace: 2 splits of 1504 tokens
+    assert pkv.decode_plan(cache, 8, small) == (1504, 2)
+    o = pkv.paged_decode(cache, 0, q, workspace=small)
+    assert_close(f64(o), oracle_decode(case), "bf16", "2-split plan")
+
+
+def test_decode_step_replays_in_a_cuda_graph():
+    """kv_write + decode captured once, replayed with metadata updated in place."""
+    case = W.batched_decode(batch=8, lo=100, hi=700, size=16384, seed=515)
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    o = torch.empty_like(q)
+    chunk = 64
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkv.kv_write(cache, case.layer_id, kn, vn, stream=s)
+        pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws, chunk=chunk, stream=s)
+    s.synchronize()
+    eager = o.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.kv_write(cache, case.layer_id, kn, vn, stream=s)
+        pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws, chunk=chunk, stream=s)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, eager)
+    # shorten every context in place and replay: matches the oracle on the new lengths
+    new_lens = np.maximum(case.seq_lens - 50, 1).astype(np.int32)
+    cache.seq_lens.copy_(torch.from_numpy(new_lens))
+    g.replay()
+    torch.cuda.synchronize()
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    ref = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                        new_lens, case.q, case.layer_id)
+    assert_close(f64(o), ref, "bf16", "graph replay with new lengths")
+    no_device_error()
