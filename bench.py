@@ -225,31 +225,28 @@ class DecodeStep:
 
 
 def timed(torch, stream, fn, steps, warmup, flush, parts=None):
-    """Run fn `warmup` times, then `steps` times with an L2 flush before each;
-    CUDA events on `stream` bracket each step (and each part, if given)."""
+    """Run the step `warmup` times, then `steps` times with an L2 flush before
+    each; CUDA events on `stream` bracket each step and each of its parts.
+    The step is fn(), or the calls in `parts` one after another."""
+    calls = list(parts) if parts else [fn]
     for _ in range(warmup):
         flush.add_(1)
-        fn()
+        for c in calls:
+            c()
     torch.cuda.synchronize()
     ev = []
-    for i in range(steps):
+    for _ in range(steps):
         flush.add_(1)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(2 + (len(parts) if parts else 0))]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(1 + len(calls))]
         e[0].record(stream)
-        if parts:
-            for j, p in enumerate(parts):
-                p()
-                e[1 + j].record(stream)
-        else:
-            fn()
-            e[1].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            e[1 + j].record(stream)
         ev.append(e)
     torch.cuda.synchronize()
     total = [e[0].elapsed_time(e[-1]) for e in ev]
-    per_part = None
-    if parts:
-        per_part = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(len(parts))]
-    return total, per_part
+    per_part = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(len(calls))]
+    return total, (per_part if parts else None)
 
 
 def run_pkv(args):
