@@ -213,6 +213,30 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
                       float sm_scale, const pkv_workspace *ws, void *stream);
 
 /*
+ * Paged decode for callers that cannot allocate device memory: code running
+ * while another component holds a stream capture open in global mode (where
+ * cudaMalloc is not allowed), plugins inside engines whose allocator owns all
+ * device memory, or latency-bound loops that cannot take cudaMalloc's
+ * implicit synchronisation.  The paper has no counterpart: its decode always
+ * receives a workspace.
+ *
+ * Same operation, arguments and results as pkv_paged_decode, but the split-K
+ * partials live in a library-owned device array of 8 MiB (a file-scope
+ * __device__ object that every GPU loading the library holds until the
+ * process exits).  Nothing is allocated or freed.  The number of splits is
+ * capped by what fits in the array for batch x n_heads x head_dim; a call
+ * that cannot fit even one split per (entry, head), or whose contexts would
+ * then need chunks over 2048 tokens, returns PKV_ERR_WORKSPACE.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the one array
+ * and leaves its partials there (nothing in it has to start at zero): calls
+ * that overlap on the GPU, on any streams, race and give wrong results.
+ */
+int pkv_paged_decode_noalloc(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                             int32_t n_heads, float sm_scale, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the calling device's error word.
  * Returns PKV_OK, PKV_ERR_INDEX (device data out of range since the last
  * read; *detail, if non-NULL, receives the first offending value) or

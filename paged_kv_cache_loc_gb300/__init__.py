@@ -12,8 +12,8 @@ Operations (AstrAI docs/guides/inference.md):
   paged_prefill   ragged causal prefill over qo_indptr / kv_indptr ("Attention Backend")
 """
 from .ops import (KVCache, Workspace, decode_plan, kv_write, last_device_error,  # noqa: F401
-                  paged_decode, paged_prefill, rope_kv_write)
+                  paged_decode, paged_decode_noalloc, paged_prefill, rope_kv_write)
 from ._lib import PkvError, load  # noqa: F401
 
 __all__ = ["KVCache", "Workspace", "kv_write", "rope_kv_write", "paged_decode", "paged_prefill",
-           "decode_plan", "last_device_error", "PkvError", "load"]
+           "paged_decode_noalloc", "decode_plan", "last_device_error", "PkvError", "load"]

@@ -79,6 +79,8 @@ SIGNATURES = {
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_float,
                                          ctypes.POINTER(PkvWorkspace), _vp]),
+    "pkv_paged_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(PkvKVCache), ctypes.c_int32, _vp,
+                                                _vp, ctypes.c_int32, ctypes.c_float, _vp]),
     "pkv_last_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int64)]),
     "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_version": (ctypes.c_char_p, []),

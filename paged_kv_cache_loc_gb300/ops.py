@@ -148,6 +148,21 @@ def paged_decode(cache: KVCache, layer_id: int, q: torch.Tensor, o: Optional[tor
     return o
 
 
+def paged_decode_noalloc(cache: KVCache, layer_id: int, q: torch.Tensor, o: torch.Tensor,
+                         sm_scale: Optional[float] = None, stream=None) -> torch.Tensor:
+    """paged_decode with the split partials in the library's fixed device array
+    (for callers that cannot allocate a workspace); o must be preallocated."""
+    c = cache.c_struct()
+    dev = cache.device
+    scale = 1.0 / math.sqrt(int(q.shape[2])) if sm_scale is None else float(sm_scale)
+    check(_lib.load().pkv_paged_decode_noalloc(ctypes.byref(c), layer_id,
+                                               _need(q, "q", cache.k_buffer.dtype, dev),
+                                               _need(o, "o", cache.k_buffer.dtype, dev),
+                                               int(q.shape[1]), scale, _stream(stream, dev)),
+          "pkv_paged_decode_noalloc")
+    return o
+
+
 def decode_plan(cache: KVCache, n_heads: int, workspace: Optional[Workspace] = None
                 ) -> Tuple[int, int]:
     """(chunk, n_splits) that paged_decode picks automatically."""
