@@ -224,19 +224,32 @@ class DecodeStep:
                                                      self.s), "pkv_paged_decode")
 
 
+def make_l2_flush(torch, dev):
+    """Evict L2 between timed steps: write a 256 MB buffer, then read another
+    256 MB so that the dirty lines of the write are written back before the
+    step starts (their write-backs are not charged to the measured kernel)."""
+    wbuf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.add_(1.0)
+        rbuf.sum()
+    return flush
+
+
 def timed(torch, stream, fn, steps, warmup, flush, parts=None):
     """Run the step `warmup` times, then `steps` times with an L2 flush before
     each; CUDA events on `stream` bracket each step and each of its parts.
     The step is fn(), or the calls in `parts` one after another."""
     calls = list(parts) if parts else [fn]
     for _ in range(warmup):
-        flush.add_(1)
+        flush()
         for c in calls:
             c()
     torch.cuda.synchronize()
     ev = []
     for _ in range(steps):
-        flush.add_(1)
+        flush()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(1 + len(calls))]
         e[0].record(stream)
         for j, c in enumerate(calls):
@@ -265,7 +278,7 @@ def run_pkv(args):
     lib = _lib.load()
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = make_l2_flush(torch, dev)
 
     # ---- the workload: batched GQA decode -------------------------------
     case = W.batched_decode(seed=1002 + 100 * rank)
@@ -274,10 +287,14 @@ def run_pkv(args):
     ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024, device=dev)
     chunk = args.chunk
     if chunk == 0:
-        chunk, _ = pkv.decode_plan(cache, case.n_heads, ws)
-    n_splits = -(-case.max_len // chunk)
+        plan_chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
+        mode = (f"balanced: {n_splits} CTAs share all tokens (kv_indptr)" if plan_chunk == 0
+                else f"chunked: {plan_chunk}-token splits")
+    else:
+        n_splits = -(-case.max_len // chunk)
+        mode = f"chunked: {chunk}-token splits"
     step = DecodeStep(lib, cache, q, kn, vn, o, ws, case.layer_id, chunk, stream)
-    launches_per_step = 1 + 1 + (0 if n_splits == 1 else 1)
+    launches_per_step = 1 + 1 + (0 if (n_splits == 1 and chunk != 0) else 1)
 
     with torch.cuda.stream(stream):
         if world > 1:
@@ -335,8 +352,8 @@ def run_pkv(args):
                    "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
                    "seq_lens": "uniform [512, 4096]", "total_kv_tokens": int(case.seq_lens.sum()),
                    "pool_slots": case.size, "n_layers": case.n_layers, "layer_id": case.layer_id,
-                   "page_size": 1, "split_chunk": chunk, "n_splits": n_splits,
-                   "l2": "flushed (256 MB write) before every timed step",
+                   "page_size": 1, "decode_plan": mode,
+                   "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": f"replicas x{world}"},
         "decode_tokens_per_s": round(world * case.batch / (total_ms * 1e-3), 1),
         "attention_stack_tokens_per_s": round(world * case.batch / (case.n_layers * total_ms * 1e-3), 1),
@@ -406,7 +423,7 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
     pkv.kv_write(cache, case.layer_id, kn, vn)
     ws = pkv.Workspace(1, case.n_heads, case.head_dim, 1024, device=dev)
     o = torch.empty_like(q)
-    chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
+    plan_chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
     with torch.cuda.stream(stream):
         ms, _ = timed(torch, stream,
                       lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
@@ -415,8 +432,10 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
     b = decode_bytes(case)
     gbs = b / (t * 1e-3) / 1e9
     return {"context": 32768, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
-            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "split_chunk": chunk,
-            "n_splits": n_splits, "algorithmic_bytes": b}
+            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+            "decode_plan": (f"balanced: {n_splits} CTAs" if plan_chunk == 0
+                            else f"chunked: {plan_chunk}-token splits"),
+            "algorithmic_bytes": b}
 
 
 def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):

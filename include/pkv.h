@@ -67,10 +67,14 @@ enum {
  *   req_pool_indices    int32 [batch]: request row of each batch entry.
  *   seq_lens            int32 [batch]: decode context length of each entry,
  *                       INCLUDING the token written this step.
- *   kv_indptr           int32 [batch + 1]: prefix sums of the kv lengths; in
- *                       prefill the kv length of entry b is
- *                       kv_indptr[b+1] - kv_indptr[b] (cached prefix + new
- *                       tokens).  Decode does not read it (may be NULL).
+ *   kv_indptr           int32 [batch + 1]: prefix sums of the kv lengths
+ *                       (kv_indptr[0] = 0); in prefill the kv length of entry b
+ *                       is kv_indptr[b+1] - kv_indptr[b] (cached prefix + new
+ *                       tokens).  In decode it is optional: when given, it
+ *                       must equal the prefix sums of seq_lens, and the
+ *                       automatic plan splits all tokens of the batch evenly
+ *                       across the SMs (an entry whose differences disagree
+ *                       with seq_lens is a device-data error).
  *   qo_indptr           int32 [batch + 1]: prefix sums of the query lengths
  *                       (prefill only; NULL in decode).
  *   out_cache_loc       int32 [n_new]: destination slot of each new token, in
@@ -170,9 +174,15 @@ int pkv_rope_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, con
  *   slot_j = c->req_to_token[r, j],  G = n_heads / c->n_kv_heads,
  * with K/V the rows of layer `layer_id`.  q, o: [batch, n_heads, head_dim] of
  * c->dtype; o must not alias q.  n = 0 gives o = 0.  Accumulation in fp32,
- * one rounding to the output dtype.  Long contexts are split into chunks
- * whose partials go to the workspace and are merged by a second kernel; the
- * split count is chosen on the host from c->max_len, c->batch and the SM count.
+ * one rounding to the output dtype.  The work is split and the partials go
+ * to the workspace, merged by a second kernel:
+ *   - with c->kv_indptr (bf16, n_kv_heads in {1, 2, 4, 8}): the tokens of the
+ *     whole batch, [0, kv_indptr[batch]), are divided evenly among up to one
+ *     CTA per SM; the workspace must hold (CTAs + batch) x n_heads partial
+ *     rows (else the chunked plan below is used);
+ *   - otherwise each context is cut into chunks whose size is chosen on the
+ *     host from c->max_len, c->batch and the SM count.
+ * Without a workspace only single-split plans are possible.
  * Supported: head_dim 64 or 128, G in {1, 2, 4, 8}.
  */
 int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
@@ -189,8 +199,10 @@ int pkv_paged_decode_chunked(const pkv_kvcache *c, int32_t layer_id, const void 
                              const pkv_workspace *ws, void *stream);
 
 /*
- * The split plan pkv_paged_decode would use: *chunk tokens per split and
- * *n_splits = ceil(c->max_len / *chunk) splits.  Host-only; enqueues nothing.
+ * The plan pkv_paged_decode would use: *chunk tokens per split and
+ * *n_splits = ceil(c->max_len / *chunk) splits, or *chunk = 0 and *n_splits =
+ * the number of CTAs when the tokens are divided evenly over kv_indptr.
+ * Host-only; enqueues nothing.
  */
 int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *ws,
                     int32_t *chunk, int32_t *n_splits);

@@ -86,29 +86,72 @@ int ws_check(const pkv_workspace *ws) {
     return PKV_OK;
 }
 
-// Split plan: about four CTAs per SM of (entry, kv head, split) work if every
-// context were max_len long, chunks of 64..2048 tokens in steps of 32, and
-// never more splits than the workspace holds.
-int plan(const pkv_kvcache *c, int sms, const pkv_workspace *ws, int32_t *chunk_out) {
+// The decode work plan.
+//  balanced: chosen when the caller asked for the automatic plan, passed
+//    kv_indptr, the shape has a balanced kernel and the workspace holds
+//    (n_parts + batch) * n_heads partial rows.  n_parts CTAs (one per SM, or
+//    fewer for small batches) share all tokens of the batch equally.
+//  chunked: each entry's context is cut into chunks; about four CTAs per SM
+//    if every context were max_len long, 64..2048 tokens in steps of 32, never
+//    more splits than the workspace holds (one split without a workspace).
+struct Plan {
+    int balanced = 0;
+    int32_t chunk = 0;
+    int32_t n_splits = 1;
+    int32_t n_parts = 0;
+};
+
+bool ws_holds(const pkv_workspace *ws, int64_t rows, int head_dim) {
+    const int64_t cap_o =
+        static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * ws->head_dim;
+    const int64_t cap_ml = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * 2;
+    return rows * head_dim <= cap_o && rows * 2 <= cap_ml;
+}
+
+int make_plan(const pkv_kvcache *c, int32_t n_heads, int sms, const pkv_workspace *ws,
+              int32_t chunk_req, Plan *out) {
     const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
-    const int64_t units = static_cast<int64_t>(c->batch > 0 ? c->batch : 1) * c->n_kv_heads;
-    const int64_t target = static_cast<int64_t>(sms > 0 ? sms : 1) * 4;
-    int64_t chunk = (max_len * units + target - 1) / target;
-    chunk = (chunk + 31) / 32 * 32;
-    if (chunk < 64) chunk = 64;
-    if (chunk > pkv::kDecodeMaxChunk) chunk = pkv::kDecodeMaxChunk;
-    int64_t cap_splits = pkv::kDecodeMaxSplits;
-    if (ws_check(ws) == PKV_OK) {
-        if (ws->max_splits < cap_splits) cap_splits = ws->max_splits;
-    } else {
-        cap_splits = 1;   // no workspace: one split per entry
+    const int64_t batch = c->batch > 0 ? c->batch : 1;
+    const int group = n_heads / c->n_kv_heads;
+    const bool have_ws = ws_check(ws) == PKV_OK;
+    if (chunk_req == 0 && c->kv_indptr && have_ws &&
+        pkv::decode_balanced_supported(c->dtype, c->head_dim, group, c->n_kv_heads)) {
+        int64_t parts = (max_len * batch + 127) / 128;   // at least ~128 tokens per CTA
+        const int64_t cap = sms > 0 ? sms : 1;
+        if (parts > cap) parts = cap;
+        if (parts < 1) parts = 1;
+        if (ws_holds(ws, (parts + batch) * n_heads, c->head_dim)) {
+            out->balanced = 1;
+            out->n_parts = static_cast<int32_t>(parts);
+            out->chunk = 0;
+            out->n_splits = static_cast<int32_t>(parts);
+            return PKV_OK;
+        }
     }
-    if ((max_len + chunk - 1) / chunk > cap_splits) {
-        chunk = (max_len + cap_splits - 1) / cap_splits;
+    int64_t chunk = chunk_req;
+    if (chunk == 0) {
+        const int64_t units = batch * c->n_kv_heads;
+        const int64_t target = static_cast<int64_t>(sms > 0 ? sms : 1) * 4;
+        chunk = (max_len * units + target - 1) / target;
         chunk = (chunk + 31) / 32 * 32;
+        if (chunk < 64) chunk = 64;
+        if (chunk > pkv::kDecodeMaxChunk) chunk = pkv::kDecodeMaxChunk;
+        const int64_t cap_splits =
+            have_ws ? (ws->max_splits < pkv::kDecodeMaxSplits ? ws->max_splits : pkv::kDecodeMaxSplits)
+                    : 1;
+        if ((max_len + chunk - 1) / chunk > cap_splits) {
+            chunk = (max_len + cap_splits - 1) / cap_splits;
+            chunk = (chunk + 31) / 32 * 32;
+        }
+        if (chunk > pkv::kDecodeMaxChunk) return PKV_ERR_WORKSPACE;
     }
-    if (chunk > pkv::kDecodeMaxChunk) return PKV_ERR_WORKSPACE;
-    *chunk_out = static_cast<int32_t>(chunk);
+    if (chunk <= 0 || chunk % 32 || chunk > pkv::kDecodeMaxChunk) return PKV_ERR_ARG;
+    const int64_t n_splits = (max_len + chunk - 1) / chunk;
+    if (n_splits > pkv::kDecodeMaxSplits) return PKV_ERR_ARG;
+    out->balanced = 0;
+    out->chunk = static_cast<int32_t>(chunk);
+    out->n_splits = static_cast<int32_t>(n_splits);
+    out->n_parts = 0;
     return PKV_OK;
 }
 
@@ -127,26 +170,22 @@ int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, 
     DeviceInfo di;
     rc = device_info(&di);
     if (rc) return rc;
-    if (chunk == 0) {
-        rc = plan(c, di.sms, ws, &chunk);
-        if (rc) return rc;
-    }
-    if (chunk <= 0 || chunk % 32 || chunk > pkv::kDecodeMaxChunk) return PKV_ERR_ARG;
-    const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
-    const int64_t n_splits = (max_len + chunk - 1) / chunk;
-    if (n_splits > pkv::kDecodeMaxSplits) return PKV_ERR_ARG;
+    Plan plan;
+    rc = make_plan(c, n_heads, di.sms, ws, chunk, &plan);
+    if (rc) return rc;
 
     pkv::DecodeParams p{};
-    p.direct = n_splits == 1;
+    p.balanced = plan.balanced;
+    p.n_parts = plan.n_parts;
+    p.kv_indptr = c->kv_indptr;
+    p.direct = !plan.balanced && plan.n_splits == 1;
     if (!p.direct) {
         rc = ws_check(ws);
         if (rc) return rc;
-        const int64_t need_o = static_cast<int64_t>(c->batch) * n_heads * n_splits * c->head_dim;
-        const int64_t cap_o = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits *
-                              ws->head_dim;
-        const int64_t need_ml = static_cast<int64_t>(c->batch) * n_heads * n_splits * 2;
-        const int64_t cap_ml = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * 2;
-        if (need_o > cap_o || need_ml > cap_ml) return PKV_ERR_WORKSPACE;
+        const int64_t rows = plan.balanced
+                                 ? (static_cast<int64_t>(plan.n_parts) + c->batch) * n_heads
+                                 : static_cast<int64_t>(c->batch) * n_heads * plan.n_splits;
+        if (!ws_holds(ws, rows, c->head_dim)) return PKV_ERR_WORKSPACE;
         p.o_part = ws->o_part;
         p.ml_part = ws->ml_part;
     }
@@ -165,8 +204,8 @@ int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, 
     p.max_ctx_len = c->max_ctx_len;
     p.batch = c->batch;
     p.max_len = c->max_len;
-    p.chunk = chunk;
-    p.n_splits = static_cast<int32_t>(n_splits);
+    p.chunk = plan.chunk;
+    p.n_splits = plan.n_splits;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.err = di.err;
     return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, group,
@@ -268,15 +307,17 @@ int pkv_paged_decode_chunked(const pkv_kvcache *c, int32_t layer_id, const void 
 
 int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *ws,
                     int32_t *chunk, int32_t *n_splits) {
-    if (!c || !chunk || !n_splits || c->n_kv_heads <= 0 || n_heads <= 0 || c->max_len < 0)
+    if (!c || !chunk || !n_splits || c->n_kv_heads <= 0 || n_heads <= 0 || c->max_len < 0 ||
+        n_heads % c->n_kv_heads)
         return PKV_ERR_ARG;
     DeviceInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
-    rc = plan(c, di.sms, ws, chunk);
+    Plan plan;
+    rc = make_plan(c, n_heads, di.sms, ws, 0, &plan);
     if (rc) return rc;
-    const int64_t max_len = c->max_len > 0 ? c->max_len : 1;
-    *n_splits = static_cast<int32_t>((max_len + *chunk - 1) / *chunk);
+    *chunk = plan.chunk;
+    *n_splits = plan.n_splits;
     return PKV_OK;
 }
 

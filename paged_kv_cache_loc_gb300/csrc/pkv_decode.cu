@@ -7,6 +7,10 @@
 //   slot_j = req_to_token[req_pool_indices[b], j].
 // The workspace partials follow the pages' decode_o_part / decode_ml_part.
 //
+// This file holds the CUDA-core split kernel (fp32 storage), the merge
+// kernel shared by both dtypes, and the dispatch; bf16 storage runs its split
+// pass on tensor cores (pkv_decode_mma.cu).
+//
 // Design (memory-bound): one CTA per (split, kv head, entry).  Its G query
 // heads share every K/V row it reads, so each row leaves HBM once per call.
 //   1. the split's int32 slot indices are staged in shared memory once;
@@ -24,6 +28,7 @@
 #include <float.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pkv_common.cuh"
 #include "pkv_launch.h"
@@ -402,6 +407,15 @@ __global__ void __launch_bounds__(kNT) decode_merge_kernel(const DecodeParams p)
 template <typename T, int D, int G>
 cudaError_t run(const DecodeParams &p, cudaStream_t s) {
     using C = DecodeCfg<T, D, G>;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        // bf16: the split pass runs on tensor cores
+        cudaError_t e = launch_decode_split_mma(p, D, G, s);
+        if (e != cudaSuccess) return e;
+        if (p.balanced) return launch_decode_merge_balanced(p, D, s);
+        if (p.direct) return cudaSuccess;
+        decode_merge_kernel<T, D><<<p.batch * p.n_heads, kNT, 0, s>>>(p);
+        return cudaGetLastError();
+    } else {
     static std::atomic<uint64_t> attr_done{0};   // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -420,6 +434,7 @@ cudaError_t run(const DecodeParams &p, cudaStream_t s) {
     if (e != cudaSuccess || p.direct) return e;
     decode_merge_kernel<T, D><<<p.batch * p.n_heads, kNT, 0, s>>>(p);
     return cudaGetLastError();
+    }
 }
 
 template <typename T, int D>

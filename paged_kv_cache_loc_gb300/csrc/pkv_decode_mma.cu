@@ -1,0 +1,776 @@
+// pkv_decode_mma.cu -- bf16 paged decode on tensor cores (split pass).
+//
+// Same operation and workspace contract as the split kernel in
+// pkv_decode.cu (AstrAI docs/guides/inference.md, "KV Cache" formula read
+// through req_to_token, "Attention Backend" decode path); this is the bf16
+// path.  The G query heads that share a kv head make the score block a real
+// matrix product, so both products run as mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) with the heads as the N = 8 dimension:
+//   S^T[16 tokens x 8 heads]  = K[16 x D] . Q^T[D x 8]       (A = K from smem)
+//   O^T[D x 8 heads]         += V^T[D x 16] . P^T[16 x 8]     (A = V^T via ldmatrix.trans)
+// P^T goes from the accumulator layout to the B-operand layout with two
+// movmatrix transposes, so probabilities never touch shared memory.
+//
+// Two kernels share these building blocks:
+//  - decode_mma_kernel: one CTA per (split, kv head, entry), four warps each
+//    running its own cp.async ring over interleaved 16-token blocks; used
+//    when n_kv_heads does not divide 8;
+//  - decode_mma_allheads_kernel: one CTA reads whole slot rows of all kv
+//    heads (below), either per (split, entry) or over an exactly balanced
+//    partition of all tokens of the batch.
+// Rows are XOR-swizzled in shared memory so that ldmatrix is free of bank
+// conflicts; per-warp (m, l, O) are combined in shared memory at the end.
+#include <atomic>
+
+#include "pkv_common.cuh"
+#include "pkv_launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kNT = kWarps * 32;
+constexpr int kBlk = 16;          // tokens per block (the mma M / K extent)
+
+template <int D>
+struct MmaCfg {
+    static constexpr int kStages = 3;
+    static constexpr int kChunks = D / 8;                        // 16-byte chunks per row
+    static constexpr int kBlkElems = kBlk * D;                   // one K (or V) block
+    static constexpr int kStageElems = 2 * kBlkElems;            // K + V
+    static constexpr size_t kSlotBytes = kDecodeMaxChunk * 4;
+    static constexpr size_t kRingBytes = static_cast<size_t>(kWarps) * kStages * kStageElems * 2;
+    static constexpr size_t kSmem = kSlotBytes + kRingBytes;
+    static constexpr int kCpPerLane = 2 * kBlk * kChunks / 32;   // cp.async per lane per block
+};
+
+__device__ __forceinline__ int swz(int row, int chunk, int d) {
+    return row * d + ((chunk ^ (row & 7)) << 3);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kNT, 2) decode_mma_kernel(const DecodeParams p) {
+    using C = MmaCfg<D>;
+    using bf16 = __nv_bfloat16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    int *slots = reinterpret_cast<int *>(smem);
+    bf16 *ring_all = reinterpret_cast<bf16 *>(smem + C::kSlotBytes);
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    int r = __ldg(p.req_pool_indices + b);
+    if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+        record_error(p.err, r);
+        r = 0;
+    }
+    int n = __ldg(p.seq_lens + b);
+    const int n_cap = min(p.max_len, p.max_ctx_len);
+    if (n < 0 || n > n_cap) {
+        record_error(p.err, n);
+        n = max(0, min(n, n_cap));
+    }
+    const int start = split * p.chunk;
+    if (start >= n) {
+        if (p.direct && n == 0) {
+            bf16 *o = static_cast<bf16 *>(p.o) + (static_cast<int64_t>(b) * p.n_heads + g * G) * D;
+            for (int i = tid; i < G * D; i += kNT) o[i] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    const int len = min(p.chunk, n - start);
+
+    const int32_t *row = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len + start;
+    for (int j = tid; j < len; j += kNT) {
+        int sl = __ldg(row + j);
+        if (static_cast<unsigned long long>(static_cast<long long>(sl)) >=
+            static_cast<unsigned long long>(p.size)) {
+            record_error(p.err, sl);
+            sl = 0;
+        }
+        slots[j] = sl;
+    }
+
+    // Q^T B-fragments: lane holds head lane/4, dims ks*16 + 2*(lane%4) + {0,1} (+8)
+    uint32_t qb[D / 16][2];
+    {
+        const int h = lane >> 2;
+        const bf16 *qrow = static_cast<const bf16 *>(p.q) +
+                           (static_cast<int64_t>(b) * p.n_heads + g * G + (h < G ? h : 0)) * D +
+                           2 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qb[ks][0] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16) : 0u;
+            qb[ks][1] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8) : 0u;
+        }
+    }
+    __syncthreads();
+
+    const int64_t slot_stride = static_cast<int64_t>(p.n_kv_heads) * D;
+    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + (p.layer_row0 * p.n_kv_heads + g) * D;
+    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + (p.layer_row0 * p.n_kv_heads + g) * D;
+    bf16 *ring = ring_all + static_cast<size_t>(warp) * C::kStages * C::kStageElems;
+
+    const int nblk = (len + kBlk - 1) / kBlk;
+    const int cnt = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+
+    // issue the copies of this warp's k-th block into ring stage `st`
+    auto issue = [&](int k, int st) {
+        const int t0 = (warp + k * kWarps) * kBlk;
+        bf16 *dst0 = ring + st * C::kStageElems;
+#pragma unroll
+        for (int i = 0; i < C::kCpPerLane; ++i) {
+            const int idx = lane + 32 * i;
+            const int kv = idx / (kBlk * C::kChunks);
+            const int rem = idx - kv * (kBlk * C::kChunks);
+            const int t = rem / C::kChunks;
+            const int c = rem - t * C::kChunks;
+            bf16 *dst = dst0 + kv * C::kBlkElems + swz(t, c, D);
+            const int tok = t0 + t;
+            if (tok < len) {
+                cp_async16(dst, (kv ? vbase : kbase) + slots[tok] * slot_stride + c * 8);
+            } else {
+                cp_async16(dst, kbase, 0);
+            }
+        }
+    };
+
+#pragma unroll
+    for (int st = 0; st < C::kStages - 1; ++st) {
+        if (st < cnt) issue(st, st);
+        cp_async_commit();
+    }
+
+    float o_acc[D / 16][4];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;   // running max, heads 2*(lane%4) and +1
+    float l0 = 0.f, l1 = 0.f;               // lane-partial denominators
+
+    for (int k = 0; k < cnt; ++k) {
+        cp_async_wait<C::kStages - 2>();
+        __syncwarp();
+        if (k + C::kStages - 1 < cnt) issue(k + C::kStages - 1, (k + C::kStages - 1) % C::kStages);
+        cp_async_commit();
+
+        const bf16 *kt = ring + (k % C::kStages) * C::kStageElems;
+        const bf16 *vt = kt + C::kBlkElems;
+        const int valid = len - (warp + k * kWarps) * kBlk;   // >= 1
+
+        // S^T = K Q^T
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, kt + swz(lane & 15, 2 * ks + (lane >> 4), D));
+            mma16816(s, a, qb[ks][0], qb[ks][1]);
+        }
+        const int tA = lane >> 2, tB = tA + 8;
+        s[0] = tA < valid ? s[0] * p.scale_log2 : -INFINITY;
+        s[1] = tA < valid ? s[1] * p.scale_log2 : -INFINITY;
+        s[2] = tB < valid ? s[2] * p.scale_log2 : -INFINITY;
+        s[3] = tB < valid ? s[3] * p.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+        l0 = l0 * al0 + p0 + p2;
+        l1 = l1 * al1 + p1 + p3;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                o_acc[i][0] *= al0;
+                o_acc[i][1] *= al1;
+                o_acc[i][2] *= al0;
+                o_acc[i][3] *= al1;
+            }
+        }
+        // P^T (tokens x heads) -> B fragments (k = tokens, n = heads)
+        const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+        const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+        // O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_t(a, vt + swz((lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1), D));
+            mma16816(o_acc[mt], a, pb0, pb1);
+        }
+    }
+    cp_async_wait<0>();
+
+    // denominators: sum the lane partials over the 8 lanes sharing a head pair
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+
+    // combine the warps: red_o[w][h][D], red_ml[w][h][2]
+    __syncthreads();
+    float *red_o = reinterpret_cast<float *>(ring_all);
+    float *red_ml = red_o + kWarps * G * D;
+    const int h0 = 2 * (lane & 3), h1 = h0 + 1;
+    if (lane < 4) {
+        if (h0 < G) {
+            red_ml[(warp * G + h0) * 2] = m0;
+            red_ml[(warp * G + h0) * 2 + 1] = l0;
+        }
+        if (h1 < G) {
+            red_ml[(warp * G + h1) * 2] = m1;
+            red_ml[(warp * G + h1) * 2 + 1] = l1;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int d0 = mt * 16 + (lane >> 2);
+        if (h0 < G) {
+            red_o[(warp * G + h0) * D + d0] = o_acc[mt][0];
+            red_o[(warp * G + h0) * D + d0 + 8] = o_acc[mt][2];
+        }
+        if (h1 < G) {
+            red_o[(warp * G + h1) * D + d0] = o_acc[mt][1];
+            red_o[(warp * G + h1) * D + d0 + 8] = o_acc[mt][3];
+        }
+    }
+    __syncthreads();
+
+    const int64_t bh0 = static_cast<int64_t>(b) * p.n_heads + g * G;
+    for (int i = tid; i < G * D; i += kNT) {
+        const int h = i / D, e = i - (i / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[(w * G + h) * 2]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float sc = exp2f(red_ml[(w * G + h) * 2] - M);
+            L += red_ml[(w * G + h) * 2 + 1] * sc;
+            O += red_o[(w * G + h) * D + e] * sc;
+        }
+        const float out = O / L;
+        if (p.direct) {
+            static_cast<bf16 *>(p.o)[(bh0 + h) * D + e] = __float2bfloat16_rn(out);
+        } else {
+            const int64_t ps = (bh0 + h) * p.n_splits + split;
+            p.o_part[ps * D + e] = out;
+            if (e == 0) {
+                p.ml_part[ps * 2] = M;
+                p.ml_part[ps * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// All kv heads in one CTA.  A stage holds TS = 128 / HK tokens of every kv
+// head, so each slot's K (and V) row of n_kv_heads * D elements is fetched as
+// one contiguous run (2 KB for 8 heads of 128 bf16) rather than as a 256-byte
+// slice per CTA.  Warp w owns kv head w % HK and the 16-token block w / HK of
+// each stage; warps that share a head are combined at the end of a segment.
+//
+// Two ways to hand out work:
+//  - chunked: CTA (split, entry) takes tokens [split*chunk, (split+1)*chunk)
+//    of one entry;
+//  - balanced: the grid is n_parts CTAs over the flattened token space
+//    [0, T), T = kv_indptr[batch]; CTA c takes [T*c/P, T*(c+1)/P) with
+//    P = min(n_parts, T), walking across entries.  Its piece of entry b goes
+//    to partial row (c + b) (rows are unique because pieces are ordered), or
+//    straight to o when the piece is the whole entry.
+template <int D, int HK>
+struct AllHeadsCfg {
+    static constexpr int kWarpsAH = 8;
+    static constexpr int kNTAH = kWarpsAH * 32;
+    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kTS = kBlk * (kWarpsAH / HK);              // tokens per stage
+    static constexpr int kChunks = D / 8;
+    static constexpr int kHeadElems = kTS * D;                      // one head's K block
+    static constexpr int kStageElems = 2 * HK * kHeadElems;         // K and V, all heads
+    static constexpr size_t kSlotBytes = kDecodeMaxChunk * 4;
+    static constexpr size_t kSmem = kSlotBytes + static_cast<size_t>(kStages) * kStageElems * 2;
+    static constexpr int kCpPerThread = 2 * kTS * HK * kChunks / kNTAH;
+    static_assert(kWarpsAH % HK == 0, "HK must divide 8");
+};
+
+// First CTA index of the balanced partition whose range holds token t.
+__device__ __forceinline__ int part_of(long long t, long long T, int P) {
+    const long long c = ((t + 1) * P - 1) / T;
+    return static_cast<int>(c < P - 1 ? c : P - 1);
+}
+
+template <int D, int G, int HK>
+__global__ void __launch_bounds__(AllHeadsCfg<D, HK>::kNTAH, 1)
+decode_mma_allheads_kernel(const DecodeParams p) {
+    using C = AllHeadsCfg<D, HK>;
+    using bf16 = __nv_bfloat16;
+    constexpr int NW = C::kWarpsAH, NT = C::kNTAH;
+    extern __shared__ __align__(128) unsigned char smem[];
+    int *slots = reinterpret_cast<int *>(smem);
+    bf16 *ring = reinterpret_cast<bf16 *>(smem + C::kSlotBytes);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hw = warp % HK;          // this warp's kv head
+    const int blk = warp / HK;         // this warp's 16-token block within a stage
+    const int n_cap = min(p.max_len, p.max_ctx_len);
+    const int64_t slot_stride = static_cast<int64_t>(HK) * D;
+    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + p.layer_row0 * slot_stride;
+    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + p.layer_row0 * slot_stride;
+
+    // Process positions [s0, s1) of entry b (request row r) and write the
+    // result to o (direct) or to partial row `prow` (n_heads rows per index).
+    auto segment = [&](int b, int r, int s0, int s1, bool direct, int64_t prow, int64_t pstride) {
+        uint32_t qb[D / 16][2];
+        {
+            const int h = lane >> 2;
+            const bf16 *qrow = static_cast<const bf16 *>(p.q) +
+                               (static_cast<int64_t>(b) * p.n_heads + hw * G + (h < G ? h : 0)) * D +
+                               2 * (lane & 3);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qb[ks][0] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16) : 0u;
+                qb[ks][1] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8) : 0u;
+            }
+        }
+        float o_acc[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const int32_t *r2t = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len;
+
+        for (int pc = s0; pc < s1; pc += kDecodeMaxChunk) {
+            const int len = min(kDecodeMaxChunk, s1 - pc);
+            for (int j = tid; j < len; j += NT) {
+                int sl = __ldg(r2t + pc + j);
+                if (static_cast<unsigned long long>(static_cast<long long>(sl)) >=
+                    static_cast<unsigned long long>(p.size)) {
+                    record_error(p.err, sl);
+                    sl = 0;
+                }
+                slots[j] = sl;
+            }
+            __syncthreads();
+            const int nst = (len + C::kTS - 1) / C::kTS;
+            auto issue = [&](int k, int st) {
+                const int t0 = k * C::kTS;
+                bf16 *dst0 = ring + st * C::kStageElems;
+#pragma unroll
+                for (int i = 0; i < C::kCpPerThread; ++i) {
+                    const int idx = tid + NT * i;
+                    const int kv = idx / (C::kTS * HK * C::kChunks);
+                    const int rem = idx - kv * (C::kTS * HK * C::kChunks);
+                    const int t = rem / (HK * C::kChunks);
+                    const int c = rem - t * (HK * C::kChunks);   // chunk within the all-heads row
+                    const int hh = c / C::kChunks, cc = c - hh * C::kChunks;
+                    bf16 *dst = dst0 + kv * (HK * C::kHeadElems) + hh * C::kHeadElems + swz(t, cc, D);
+                    const int tok = t0 + t;
+                    if (tok < len) {
+                        cp_async16(dst, (kv ? vbase : kbase) + slots[tok] * slot_stride + c * 8);
+                    } else {
+                        cp_async16(dst, kbase, 0);
+                    }
+                }
+            };
+#pragma unroll
+            for (int st = 0; st < C::kStages - 1; ++st) {
+                if (st < nst) issue(st, st);
+                cp_async_commit();
+            }
+            for (int k = 0; k < nst; ++k) {
+                cp_async_wait<C::kStages - 2>();
+                __syncthreads();
+                if (k + C::kStages - 1 < nst) issue(k + C::kStages - 1, (k + C::kStages - 1) % C::kStages);
+                cp_async_commit();
+
+                const int valid = len - (k * C::kTS + blk * kBlk);
+                if (valid <= 0) continue;   // warp-uniform
+                const bf16 *kt = ring + (k % C::kStages) * C::kStageElems + hw * C::kHeadElems;
+                const bf16 *vt = kt + HK * C::kHeadElems;
+                const int r0 = blk * kBlk;
+
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t a[4];
+                    ldsm_x4(a, kt + swz(r0 + (lane & 15), 2 * ks + (lane >> 4), D));
+                    mma16816(s, a, qb[ks][0], qb[ks][1]);
+                }
+                const int tA = lane >> 2, tB = tA + 8;
+                s[0] = tA < valid ? s[0] * p.scale_log2 : -INFINITY;
+                s[1] = tA < valid ? s[1] * p.scale_log2 : -INFINITY;
+                s[2] = tB < valid ? s[2] * p.scale_log2 : -INFINITY;
+                s[3] = tB < valid ? s[3] * p.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+                const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+                l0 = l0 * al0 + p0 + p2;
+                l1 = l1 * al1 + p1 + p3;
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        o_acc[i][0] *= al0;
+                        o_acc[i][1] *= al1;
+                        o_acc[i][2] *= al0;
+                        o_acc[i][3] *= al1;
+                    }
+                }
+                const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4_t(a, vt + swz(r0 + (lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1), D));
+                    mma16816(o_acc[mt], a, pb0, pb1);
+                }
+            }
+            cp_async_wait<0>();
+            __syncthreads();   // ring and slots are free for the next piece / the combine
+        }
+
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        float *red_o = reinterpret_cast<float *>(ring);   // [NW][G][D]
+        float *red_ml = red_o + NW * G * D;               // [NW][G][2]
+        const int h0 = 2 * (lane & 3), h1 = h0 + 1;
+        if (lane < 4) {
+            if (h0 < G) {
+                red_ml[(warp * G + h0) * 2] = m0;
+                red_ml[(warp * G + h0) * 2 + 1] = l0;
+            }
+            if (h1 < G) {
+                red_ml[(warp * G + h1) * 2] = m1;
+                red_ml[(warp * G + h1) * 2 + 1] = l1;
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int d0 = mt * 16 + (lane >> 2);
+            if (h0 < G) {
+                red_o[(warp * G + h0) * D + d0] = o_acc[mt][0];
+                red_o[(warp * G + h0) * D + d0 + 8] = o_acc[mt][2];
+            }
+            if (h1 < G) {
+                red_o[(warp * G + h1) * D + d0] = o_acc[mt][1];
+                red_o[(warp * G + h1) * D + d0 + 8] = o_acc[mt][3];
+            }
+        }
+        __syncthreads();
+        const int64_t bh0 = static_cast<int64_t>(b) * p.n_heads;
+        for (int i = tid; i < HK * G * D; i += NT) {
+            const int gh = i / D, e = i - gh * D;
+            const int g = gh / G, h = gh - g * G;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = g; w < NW; w += HK) M = fmaxf(M, red_ml[(w * G + h) * 2]);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = g; w < NW; w += HK) {
+                const float sc = exp2f(red_ml[(w * G + h) * 2] - M);
+                L += red_ml[(w * G + h) * 2 + 1] * sc;
+                O += red_o[(w * G + h) * D + e] * sc;
+            }
+            const float out = O / L;
+            if (direct) {
+                static_cast<bf16 *>(p.o)[(bh0 + gh) * D + e] = __float2bfloat16_rn(out);
+            } else {
+                const int64_t ps = prow + gh * pstride;
+                p.o_part[ps * D + e] = out;
+                if (e == 0) {
+                    p.ml_part[ps * 2] = M;
+                    p.ml_part[ps * 2 + 1] = L;
+                }
+            }
+        }
+        __syncthreads();   // the combine area is the ring of the next segment
+    };
+
+    if (!p.balanced) {
+        const int split = blockIdx.x, b = blockIdx.y;
+        int r = __ldg(p.req_pool_indices + b);
+        if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+            record_error(p.err, r);
+            r = 0;
+        }
+        int n = __ldg(p.seq_lens + b);
+        if (n < 0 || n > n_cap) {
+            record_error(p.err, n);
+            n = max(0, min(n, n_cap));
+        }
+        const int start = split * p.chunk;
+        if (start >= n) {
+            if (p.direct && n == 0) {
+                bf16 *o = static_cast<bf16 *>(p.o) + static_cast<int64_t>(b) * p.n_heads * D;
+                for (int i = tid; i < p.n_heads * D; i += NT) o[i] = __float2bfloat16_rn(0.f);
+            }
+            return;
+        }
+        segment(b, r, start, min(n, start + p.chunk), p.direct != 0,
+                static_cast<int64_t>(b) * p.n_heads * p.n_splits + split, p.n_splits);
+        return;
+    }
+
+    // balanced partition of [0, T)
+    const long long T = __ldg(p.kv_indptr + p.batch);
+    if (T <= 0) return;
+    const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
+    const int c = blockIdx.x;
+    if (c >= P) return;
+    long long t0 = T * c / P;
+    const long long t1 = T * (c + 1) / P;
+    int lo_b = 0, hi_b = p.batch - 1;   // first entry whose range ends after t0
+    while (lo_b < hi_b) {
+        const int mid = (lo_b + hi_b) >> 1;
+        if (__ldg(p.kv_indptr + mid + 1) > t0) hi_b = mid; else lo_b = mid + 1;
+    }
+    for (int b = lo_b; b < p.batch && t0 < t1; ++b) {
+        const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+        if (hi <= t0) continue;
+        const long long n = hi - lo;
+        int r = __ldg(p.req_pool_indices + b);
+        if (n != __ldg(p.seq_lens + b) || n > n_cap || lo < 0 ||
+            static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+            record_error(p.err, n);
+            t0 = hi;
+            continue;
+        }
+        const int s0 = static_cast<int>(t0 - lo);
+        const int s1 = static_cast<int>(min(t1, hi) - lo);
+        const bool whole = s0 == 0 && s1 == n;
+        segment(b, r, s0, s1, whole, (static_cast<int64_t>(c) + b) * p.n_heads, 1);
+        t0 = lo + s1;
+    }
+}
+
+template <int D, int G, int HK>
+cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
+    using C = AllHeadsCfg<D, HK>;
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        e = cudaFuncSetAttribute(decode_mma_allheads_kernel<D, G, HK>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(C::kSmem));
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
+    dim3 grid = p.balanced ? dim3(p.n_parts, 1) : dim3(p.n_splits, p.batch);
+    decode_mma_allheads_kernel<D, G, HK><<<grid, C::kNTAH, C::kSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t run_hk(const DecodeParams &p, cudaStream_t s) {
+    switch (p.n_kv_heads) {
+        case 1: return run_allheads<D, G, 1>(p, s);
+        case 2: return run_allheads<D, G, 2>(p, s);
+        case 4: return run_allheads<D, G, 4>(p, s);
+        case 8: return run_allheads<D, G, 8>(p, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+// Merge of the balanced mode: one CTA per (entry, head).  The entry's pieces
+// are partial rows c + b for c in [part_of(lo), part_of(hi - 1)]; a single
+// piece was written to o by the split kernel.  8 warps take every 8th piece,
+// lanes hold float4 columns, four pieces in flight per warp.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const DecodeParams p) {
+    constexpr int NT = 256, NW = 8, kCols = D / 4;
+    __shared__ float wts[kDecodeMaxSplits];
+    __shared__ float red[NW];
+    __shared__ float4 part[NW][kCols];
+    const int bh = blockIdx.x;
+    const int b = bh / p.n_heads, h = bh - b * p.n_heads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.o) + static_cast<int64_t>(bh) * D;
+
+    const long long T = __ldg(p.kv_indptr + p.batch);
+    const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+    const long long n = hi - lo;
+    const int n_cap = min(p.max_len, p.max_ctx_len);
+    const bool ok = T > 0 && n > 0 && n == __ldg(p.seq_lens + b) && n <= n_cap && lo >= 0 && hi <= T;
+    if (!ok) {   // empty (or rejected) entry: o = 0
+        for (int e = tid; e < D; e += NT) out[e] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
+    const int c_lo = part_of(lo, T, P), c_hi = part_of(hi - 1, T, P);
+    if (c_lo == c_hi) return;   // one piece: written by the split kernel
+    const int np = c_hi - c_lo + 1;
+    const int64_t row0 = (static_cast<int64_t>(c_lo) + b) * p.n_heads + h;
+
+    // piece j of this entry is partial row (c_lo + j + b) * n_heads + h
+    float mx = -INFINITY;
+    for (int j = tid; j < np; j += NT) mx = fmaxf(mx, p.ml_part[(row0 + static_cast<int64_t>(j) * p.n_heads) * 2]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int j = tid; j < np; j += NT) {
+        const int64_t rr = row0 + static_cast<int64_t>(j) * p.n_heads;
+        const float w = p.ml_part[rr * 2 + 1] * exp2f(p.ml_part[rr * 2] - M);
+        wts[j] = w;
+        sum += w;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) L += red[w];
+
+    if (lane < kCols) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        int j = warp;
+        for (; j + 3 * NW < np; j += 4 * NW) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[u] = *reinterpret_cast<const float4 *>(
+                    p.o_part + (row0 + static_cast<int64_t>(j + u * NW) * p.n_heads) * D + lane * 4);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float w = wts[j + u * NW];
+                a.x = fmaf(w, x[u].x, a.x);
+                a.y = fmaf(w, x[u].y, a.y);
+                a.z = fmaf(w, x[u].z, a.z);
+                a.w = fmaf(w, x[u].w, a.w);
+            }
+        }
+        for (; j < np; j += NW) {
+            const float4 x = *reinterpret_cast<const float4 *>(
+                p.o_part + (row0 + static_cast<int64_t>(j) * p.n_heads) * D + lane * 4);
+            const float w = wts[j];
+            a.x = fmaf(w, x.x, a.x);
+            a.y = fmaf(w, x.y, a.y);
+            a.z = fmaf(w, x.z, a.z);
+            a.w = fmaf(w, x.w, a.w);
+        }
+        part[warp][lane] = a;
+    }
+    __syncthreads();
+    if (tid < kCols) {
+        float4 t = part[0][tid];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+            t.x += part[w][tid].x;
+            t.y += part[w][tid].y;
+            t.z += part[w][tid].z;
+            t.w += part[w][tid].w;
+        }
+        const float inv = 1.f / L;
+        __nv_bfloat162 v0 = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+        __nv_bfloat162 v1 = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(out + tid * 4) = v0;
+        *reinterpret_cast<__nv_bfloat162 *>(out + tid * 4 + 2) = v1;
+    }
+}
+
+template <int D, int G>
+cudaError_t run(const DecodeParams &p, cudaStream_t s) {
+    using C = MmaCfg<D>;
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        e = cudaFuncSetAttribute(decode_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(C::kSmem));
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
+    if (p.n_kv_heads == 1 || p.n_kv_heads == 2 || p.n_kv_heads == 4 || p.n_kv_heads == 8)
+        return run_hk<D, G>(p, s);
+    dim3 grid(p.n_splits, p.n_kv_heads, p.batch);
+    decode_mma_kernel<D, G><<<grid, kNT, C::kSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_group(const DecodeParams &p, int group, cudaStream_t s) {
+    switch (group) {
+        case 1: return run<D, 1>(p, s);
+        case 2: return run<D, 2>(p, s);
+        case 4: return run<D, 4>(p, s);
+        case 8: return run<D, 8>(p, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+bool decode_balanced_supported(int dtype, int head_dim, int group, int n_kv_heads) {
+    return dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) &&
+           (group == 1 || group == 2 || group == 4 || group == 8) &&
+           (n_kv_heads == 1 || n_kv_heads == 2 || n_kv_heads == 4 || n_kv_heads == 8);
+}
+
+cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cudaStream_t s) {
+    if (head_dim == 128)
+        decode_merge_balanced_kernel<128><<<p.batch * p.n_heads, 256, 0, s>>>(p);
+    else
+        decode_merge_balanced_kernel<64><<<p.batch * p.n_heads, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_split_mma(const DecodeParams &p, int head_dim, int group,
+                                    cudaStream_t s) {
+    return head_dim == 128 ? run_group<128>(p, group, s) : run_group<64>(p, group, s);
+}
+
+}  // namespace pkv

@@ -52,6 +52,12 @@ struct DecodeParams {
     int32_t direct;             // 1: single split, write o directly (no merge)
     float scale_log2;           // sm_scale * log2(e)
     DevErr *err;
+    // Balanced mode: the split grid is n_parts CTAs that share the flattened
+    // token space [0, kv_indptr[batch]) equally; CTA c's piece of entry b is
+    // partial row (c + b) of o_part / ml_part ([n_parts + batch, n_heads, ...]).
+    const int32_t *kv_indptr;
+    int32_t balanced;
+    int32_t n_parts;
 };
 
 // Ragged causal prefill.
@@ -78,7 +84,7 @@ struct PrefillParams {
     DevErr *err;
 };
 
-constexpr int kDecodeMaxChunk = 2048;   // slot indices staged per split
+constexpr int kDecodeMaxChunk = 2048;   // slot indices staged per split (or per piece)
 constexpr int kDecodeMaxSplits = 1024;  // merge kernel limit
 
 // Each returns cudaSuccess or the launch error.  Unsupported variants return
@@ -88,6 +94,14 @@ cudaError_t launch_rope_kv_write(const KvWriteParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, int group,
                           cudaStream_t s);
 bool decode_supported(int dtype, int head_dim, int group);
+// bf16 split pass on tensor cores (pkv_decode_mma.cu); the merge is launched
+// by launch_decode.
+cudaError_t launch_decode_split_mma(const DecodeParams &p, int head_dim, int group,
+                                    cudaStream_t s);
+// Whether the bf16 balanced mode is available for this shape.
+bool decode_balanced_supported(int dtype, int head_dim, int group, int n_kv_heads);
+// Merge of the balanced mode (pkv_decode_mma.cu).
+cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group,
                            cudaStream_t s);
 bool prefill_supported(int dtype, int head_dim, int group);

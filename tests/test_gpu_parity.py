@@ -338,3 +338,42 @@ def test_decode_step_replays_in_a_cuda_graph():
                         new_lens, case.q, case.layer_id)
     assert_close(f64(o), ref, "bf16", "graph replay with new lengths")
     no_device_error()
+
+
+def test_balanced_decode_replays_in_a_cuda_graph():
+    """The automatic (balanced over kv_indptr) plan, captured once and replayed
+    after seq_lens and kv_indptr are updated in place."""
+    case = W.batched_decode(batch=12, lo=50, hi=2500, size=32768, seed=616)
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    assert pkv.decode_plan(cache, case.n_heads, ws)[0] == 0      # balanced
+    o = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkv.kv_write(cache, case.layer_id, kn, vn, stream=s)
+        pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws, stream=s)
+    s.synchronize()
+    eager = o.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.kv_write(cache, case.layer_id, kn, vn, stream=s)
+        pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws, stream=s)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, eager)
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    rng = np.random.Generator(np.random.PCG64(7))
+    new_lens = np.maximum(case.seq_lens - rng.integers(0, 400, case.batch), 0).astype(np.int32)
+    new_lens[3] = 0
+    new_indptr = np.concatenate([[0], np.cumsum(new_lens)]).astype(np.int32)
+    cache.seq_lens.copy_(torch.from_numpy(new_lens))
+    cache.kv_indptr.copy_(torch.from_numpy(new_indptr))
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    ref = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                        new_lens, case.q, case.layer_id, kv_indptr=new_indptr)
+    assert_close(f64(o), ref, "bf16", "balanced graph replay")
