@@ -76,6 +76,40 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// Bounded wait for the phase with the given parity.  Gives up after 2^18
+// polls (each poll itself waits a short hardware-defined time) and returns
+// false; the caller then records an error and stops waiting instead of
+// hanging.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < (1 << 18); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// One bulk (TMA) copy of `bytes` contiguous bytes global -> shared, counted
+// on the mbarrier `bar`.  Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kNT, 2) decode_mma_kernel(const DecodeParams p) {
     using C = MmaCfg<D>;
@@ -315,15 +349,19 @@ template <int D, int HK>
 struct AllHeadsCfg {
     static constexpr int kWarpsAH = 8;
     static constexpr int kNTAH = kWarpsAH * 32;
-    static constexpr int kStages = D == 128 ? 3 : 4;
     static constexpr int kTS = kBlk * (kWarpsAH / HK);              // tokens per stage
-    static constexpr int kChunks = D / 8;
-    static constexpr int kHeadElems = kTS * D;                      // one head's K block
-    static constexpr int kStageElems = 2 * HK * kHeadElems;         // K and V, all heads
+    static constexpr int kRowElems = HK * D;                        // one slot row, all heads
+    static constexpr int kRowBytes = kRowElems * 2;
+    static constexpr int kPitch = kRowElems + 8;                    // +16 B: ldmatrix rows hit distinct banks
+    static constexpr int kPartElems = kTS * kPitch;                 // the K (or V) part of a stage
+    static constexpr int kStageElems = 2 * kPartElems;
+    static constexpr size_t kStageBytes = static_cast<size_t>(kStageElems) * 2;
+    static constexpr int kStages = 3;
     static constexpr size_t kSlotBytes = kDecodeMaxChunk * 4;
-    static constexpr size_t kSmem = kSlotBytes + static_cast<size_t>(kStages) * kStageElems * 2;
-    static constexpr int kCpPerThread = 2 * kTS * HK * kChunks / kNTAH;
+    static constexpr size_t kBarBytes = 64;
+    static constexpr size_t kSmem = kSlotBytes + kBarBytes + kStages * kStageBytes;
     static_assert(kWarpsAH % HK == 0, "HK must divide 8");
+    static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0, "bulk copies move 16-byte units");
 };
 
 // First CTA index of the balanced partition whose range holds token t.
@@ -340,9 +378,21 @@ decode_mma_allheads_kernel(const DecodeParams p) {
     constexpr int NW = C::kWarpsAH, NT = C::kNTAH;
     extern __shared__ __align__(128) unsigned char smem[];
     int *slots = reinterpret_cast<int *>(smem);
-    bf16 *ring = reinterpret_cast<bf16 *>(smem + C::kSlotBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kSlotBytes);   // one per stage
+    bf16 *ring = reinterpret_cast<bf16 *>(smem + C::kSlotBytes + C::kBarBytes);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The merge kernel (launched as a programmatic dependent) may start its
+    // prologue now; it waits for this grid's completion before reading partials.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if (tid == 0) {
+        for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(bars + st), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    uint32_t issued = 0;               // stages issued by this CTA so far (phase bookkeeping)
+    __shared__ int s_abort;            // set once a wait gave up: no further copies or waits
+    if (tid == 0) s_abort = 0;
     const int hw = warp % HK;          // this warp's kv head
     const int blk = warp / HK;         // this warp's 16-token block within a stage
     const int n_cap = min(p.max_len, p.max_ctx_len);
@@ -384,48 +434,55 @@ decode_mma_allheads_kernel(const DecodeParams p) {
             }
             __syncthreads();
             const int nst = (len + C::kTS - 1) / C::kTS;
-            auto issue = [&](int k, int st) {
-                const int t0 = k * C::kTS;
+            const uint32_t first = issued;   // global index of this piece's stage 0
+            // Warp 0 fills stage k: every token row of K and of V is one bulk
+            // copy of all kv heads; rows past the piece repeat the first
+            // token's row so that the stage always holds finite data.
+            auto issue = [&](int k) {
+                const uint32_t g = first + k;
+                const int st = g % C::kStages;
+                const uint32_t bar = smem_u32(bars + st);
+                if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(C::kStageBytes - 2 * C::kTS * 16));
+                __syncwarp();
                 bf16 *dst0 = ring + st * C::kStageElems;
-#pragma unroll
-                for (int i = 0; i < C::kCpPerThread; ++i) {
-                    const int idx = tid + NT * i;
-                    const int kv = idx / (C::kTS * HK * C::kChunks);
-                    const int rem = idx - kv * (C::kTS * HK * C::kChunks);
-                    const int t = rem / (HK * C::kChunks);
-                    const int c = rem - t * (HK * C::kChunks);   // chunk within the all-heads row
-                    const int hh = c / C::kChunks, cc = c - hh * C::kChunks;
-                    bf16 *dst = dst0 + kv * (HK * C::kHeadElems) + hh * C::kHeadElems + swz(t, cc, D);
-                    const int tok = t0 + t;
-                    if (tok < len) {
-                        cp_async16(dst, (kv ? vbase : kbase) + slots[tok] * slot_stride + c * 8);
-                    } else {
-                        cp_async16(dst, kbase, 0);
-                    }
+                for (int i = lane; i < 2 * C::kTS; i += 32) {
+                    const int kv = i / C::kTS, t = i - kv * C::kTS;
+                    const int tok = k * C::kTS + t;
+                    const int slot = slots[tok < len ? tok : 0];
+                    bulk_g2s(smem_u32(dst0 + kv * C::kPartElems + t * C::kPitch),
+                             (kv ? vbase : kbase) + slot * slot_stride, C::kRowBytes, bar);
                 }
             };
-#pragma unroll
-            for (int st = 0; st < C::kStages - 1; ++st) {
-                if (st < nst) issue(st, st);
-                cp_async_commit();
+            if (warp == 0 && !s_abort) {
+                for (int k = 0; k < C::kStages - 1 && k < nst; ++k) issue(k);
             }
+            issued += nst;
             for (int k = 0; k < nst; ++k) {
-                cp_async_wait<C::kStages - 2>();
-                __syncthreads();
-                if (k + C::kStages - 1 < nst) issue(k + C::kStages - 1, (k + C::kStages - 1) % C::kStages);
-                cp_async_commit();
+                __syncthreads();   // stage k-1 is consumed: its buffer may be refilled
+                if (s_abort) continue;   // CTA-uniform after the barrier
+                if (warp == 0 && k + C::kStages - 1 < nst) issue(k + C::kStages - 1);
+                const uint32_t g = first + k;
+                const bool ok = __all_sync(0xffffffffu,
+                                           mbar_wait(smem_u32(bars + g % C::kStages), (g / C::kStages) & 1));
+                if (!ok) {
+                    if (lane == 0) {
+                        record_error(p.err, -1000 - k);
+                        s_abort = 1;
+                    }
+                    continue;
+                }
 
                 const int valid = len - (k * C::kTS + blk * kBlk);
                 if (valid <= 0) continue;   // warp-uniform
-                const bf16 *kt = ring + (k % C::kStages) * C::kStageElems + hw * C::kHeadElems;
-                const bf16 *vt = kt + HK * C::kHeadElems;
+                const bf16 *kt = ring + ((first + k) % C::kStages) * C::kStageElems + hw * D;
+                const bf16 *vt = kt + C::kPartElems;
                 const int r0 = blk * kBlk;
 
                 float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     uint32_t a[4];
-                    ldsm_x4(a, kt + swz(r0 + (lane & 15), 2 * ks + (lane >> 4), D));
+                    ldsm_x4(a, kt + (r0 + (lane & 15)) * C::kPitch + (2 * ks + (lane >> 4)) * 8);
                     mma16816(s, a, qb[ks][0], qb[ks][1]);
                 }
                 const int tA = lane >> 2, tB = tA + 8;
@@ -461,11 +518,11 @@ decode_mma_allheads_kernel(const DecodeParams p) {
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     uint32_t a[4];
-                    ldsm_x4_t(a, vt + swz(r0 + (lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1), D));
+                    ldsm_x4_t(a, vt + (r0 + (lane & 7) + ((lane >> 4) << 3)) * C::kPitch +
+                                     (2 * mt + ((lane >> 3) & 1)) * 8);
                     mma16816(o_acc[mt], a, pb0, pb1);
                 }
             }
-            cp_async_wait<0>();
             __syncthreads();   // ring and slots are free for the next piece / the combine
         }
 
@@ -526,7 +583,10 @@ decode_mma_allheads_kernel(const DecodeParams p) {
                 }
             }
         }
-        __syncthreads();   // the combine area is the ring of the next segment
+        // the combine area is the ring of the next segment, which the bulk
+        // copies (async proxy) will overwrite
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncthreads();
     };
 
     if (!p.balanced) {
@@ -617,106 +677,167 @@ cudaError_t run_hk(const DecodeParams &p, cudaStream_t s) {
     }
 }
 
-// Merge of the balanced mode: one CTA per (entry, head).  The entry's pieces
-// are partial rows c + b for c in [part_of(lo), part_of(hi - 1)]; a single
-// piece was written to o by the split kernel.  8 warps take every 8th piece,
-// lanes hold float4 columns, four pieces in flight per warp.
-template <int D>
+// Merge of the balanced mode.  Entry b's pieces are partial rows c + b for c
+// in [part_of(lo), part_of(hi - 1)] (a single piece was written to o by the
+// split kernel).  WPI warps merge one (entry, head): warp `sub` takes pieces
+// sub, sub + WPI, ... in batches of 32 — lane k loads (m, l) of the batch's
+// k-th piece, the batch is folded into a running (M, L, acc) with one
+// rescale, and every lane keeps float4 columns of the output with 8 piece
+// loads in flight.  WPI > 1 warps are combined through shared memory.
+template <int D, int WPI>
 __global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const DecodeParams p) {
-    constexpr int NT = 256, NW = 8, kCols = D / 4;
-    __shared__ float wts[kDecodeMaxSplits];
-    __shared__ float red[NW];
-    __shared__ float4 part[NW][kCols];
-    const int bh = blockIdx.x;
-    const int b = bh / p.n_heads, h = bh - b * p.n_heads;
+    constexpr int NW = 8, IPC = NW / WPI, kCols = D / 4;
+    __shared__ float red_ml[NW][2];
+    __shared__ float4 red_o[NW][kCols];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.o) + static_cast<int64_t>(bh) * D;
+    const int grp = warp / WPI, sub = warp % WPI;
+    const int item = blockIdx.x * IPC + grp;
+    const int n_items = p.batch * p.n_heads;
 
-    const long long T = __ldg(p.kv_indptr + p.batch);
-    const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
-    const long long n = hi - lo;
-    const int n_cap = min(p.max_len, p.max_ctx_len);
-    const bool ok = T > 0 && n > 0 && n == __ldg(p.seq_lens + b) && n <= n_cap && lo >= 0 && hi <= T;
-    if (!ok) {   // empty (or rejected) entry: o = 0
-        for (int e = tid; e < D; e += NT) out[e] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
-    const int c_lo = part_of(lo, T, P), c_hi = part_of(hi - 1, T, P);
-    if (c_lo == c_hi) return;   // one piece: written by the split kernel
-    const int np = c_hi - c_lo + 1;
-    const int64_t row0 = (static_cast<int64_t>(c_lo) + b) * p.n_heads + h;
-
-    // piece j of this entry is partial row (c_lo + j + b) * n_heads + h
-    float mx = -INFINITY;
-    for (int j = tid; j < np; j += NT) mx = fmaxf(mx, p.ml_part[(row0 + static_cast<int64_t>(j) * p.n_heads) * 2]);
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool merge = false;
+    int64_t row0 = 0;
+    __nv_bfloat16 *out = nullptr;
+    if (item < n_items) {
+        const int b = item / p.n_heads, h = item - b * p.n_heads;
+        out = static_cast<__nv_bfloat16 *>(p.o) + static_cast<int64_t>(item) * D;
+        const long long T = __ldg(p.kv_indptr + p.batch);
+        const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+        const long long n = hi - lo;
+        const int n_cap = min(p.max_len, p.max_ctx_len);
+        const bool ok = T > 0 && n > 0 && n == __ldg(p.seq_lens + b) && n <= n_cap && lo >= 0 && hi <= T;
+        if (!ok) {   // empty (or rejected) entry: o = 0
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            if (sub == 0)
+                for (int e = lane; e < D; e += 32) out[e] = __float2bfloat16_rn(0.f);
+        } else {
+            const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
+            const int c_lo = part_of(lo, T, P), c_hi = part_of(hi - 1, T, P);
+            const int np = c_hi - c_lo + 1;
+            merge = np > 1;   // one piece: written by the split kernel
+            row0 = (static_cast<int64_t>(c_lo) + b) * p.n_heads + h;
+            // the partials come from the split kernel, which may still run
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            if (merge) {
+                const int mine = np > sub ? (np - sub + WPI - 1) / WPI : 0;   // pieces of this warp
+                for (int base = 0; base < mine; base += 32) {
+                    const int k = base + lane;
+                    float m = -INFINITY, l = 0.f;
+                    if (k < mine) {
+                        const int64_t rr = row0 + static_cast<int64_t>(sub + k * WPI) * p.n_heads;
+                        m = __ldcg(p.ml_part + rr * 2);
+                        l = __ldcg(p.ml_part + rr * 2 + 1);
+                    }
+                    float bm = m;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    float M = red[0];
+                    for (int off = 16; off >= 1; off >>= 1)
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+                    const float nM = fmaxf(M, bm);
+                    const float sc = exp2f(M - nM);   // M = -inf on the first batch: 0
+                    acc.x *= sc;
+                    acc.y *= sc;
+                    acc.z *= sc;
+                    acc.w *= sc;
+                    const float w = k < mine ? l * exp2f(m - nM) : 0.f;
+                    float ws = w;
 #pragma unroll
-    for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
-    float sum = 0.f;
-    for (int j = tid; j < np; j += NT) {
-        const int64_t rr = row0 + static_cast<int64_t>(j) * p.n_heads;
-        const float w = p.ml_part[rr * 2 + 1] * exp2f(p.ml_part[rr * 2] - M);
-        wts[j] = w;
-        sum += w;
-    }
+                    for (int off = 16; off >= 1; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+                    L = L * sc + ws;
+                    M = nM;
+                    const int cnt = min(32, mine - base);
+                    for (int k0 = 0; k0 < cnt; k0 += 8) {
+                        float4 x[8];
+                        float wk[8];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    float L = 0.f;
+                        for (int u = 0; u < 8; ++u) {
+                            wk[u] = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
+                            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (k0 + u < cnt && lane < kCols) {
+                                const int64_t rr =
+                                    row0 + static_cast<int64_t>(sub + (base + k0 + u) * WPI) * p.n_heads;
+                                x[u] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + rr * D) + lane);
+                            }
+                        }
 #pragma unroll
-    for (int w = 0; w < NW; ++w) L += red[w];
-
-    if (lane < kCols) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        int j = warp;
-        for (; j + 3 * NW < np; j += 4 * NW) {
-            float4 x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                x[u] = *reinterpret_cast<const float4 *>(
-                    p.o_part + (row0 + static_cast<int64_t>(j + u * NW) * p.n_heads) * D + lane * 4);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float w = wts[j + u * NW];
-                a.x = fmaf(w, x[u].x, a.x);
-                a.y = fmaf(w, x[u].y, a.y);
-                a.z = fmaf(w, x[u].z, a.z);
-                a.w = fmaf(w, x[u].w, a.w);
+                        for (int u = 0; u < 8; ++u) {
+                            if (k0 + u < cnt) {
+                                acc.x = fmaf(wk[u], x[u].x, acc.x);
+                                acc.y = fmaf(wk[u], x[u].y, acc.y);
+                                acc.z = fmaf(wk[u], x[u].z, acc.z);
+                                acc.w = fmaf(wk[u], x[u].w, acc.w);
+                            }
+                        }
+                    }
+                }
             }
         }
-        for (; j < np; j += NW) {
-            const float4 x = *reinterpret_cast<const float4 *>(
-                p.o_part + (row0 + static_cast<int64_t>(j) * p.n_heads) * D + lane * 4);
-            const float w = wts[j];
-            a.x = fmaf(w, x.x, a.x);
-            a.y = fmaf(w, x.y, a.y);
-            a.z = fmaf(w, x.z, a.z);
-            a.w = fmaf(w, x.w, a.w);
-        }
-        part[warp][lane] = a;
     }
-    __syncthreads();
-    if (tid < kCols) {
-        float4 t = part[0][tid];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) {
-            t.x += part[w][tid].x;
-            t.y += part[w][tid].y;
-            t.z += part[w][tid].z;
-            t.w += part[w][tid].w;
+    if (WPI > 1) {
+        if (lane == 0) {
+            red_ml[warp][0] = M;
+            red_ml[warp][1] = L;
         }
+        if (lane < kCols) red_o[warp][lane] = acc;
+        __syncthreads();
+        if (sub == 0 && merge) {
+            float MM = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < WPI; ++u) MM = fmaxf(MM, red_ml[warp + u][0]);
+            float LL = 0.f;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < WPI; ++u) {
+                const float sc = exp2f(red_ml[warp + u][0] - MM);
+                LL += red_ml[warp + u][1] * sc;
+                if (lane < kCols) {
+                    const float4 t = red_o[warp + u][lane];
+                    a.x = fmaf(sc, t.x, a.x);
+                    a.y = fmaf(sc, t.y, a.y);
+                    a.z = fmaf(sc, t.z, a.z);
+                    a.w = fmaf(sc, t.w, a.w);
+                }
+            }
+            M = MM;
+            L = LL;
+            acc = a;
+        }
+    }
+    if (sub == 0 && merge && lane < kCols) {
         const float inv = 1.f / L;
-        __nv_bfloat162 v0 = __floats2bfloat162_rn(t.x * inv, t.y * inv);
-        __nv_bfloat162 v1 = __floats2bfloat162_rn(t.z * inv, t.w * inv);
-        *reinterpret_cast<__nv_bfloat162 *>(out + tid * 4) = v0;
-        *reinterpret_cast<__nv_bfloat162 *>(out + tid * 4 + 2) = v1;
+        *reinterpret_cast<__nv_bfloat162 *>(out + lane * 4) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(out + lane * 4 + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+}
+
+template <int D, int WPI>
+cudaError_t launch_merge_wpi(const DecodeParams &p, cudaStream_t s) {
+    const int items = p.batch * p.n_heads;
+    const int ipc = 8 / WPI;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((items + ipc - 1) / ipc);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_balanced_kernel<D, WPI>, p);
+}
+
+template <int D>
+cudaError_t launch_merge_d(const DecodeParams &p, cudaStream_t s) {
+    // pieces per entry are about n_parts / batch + 1: give an (entry, head)
+    // more warps when there are many
+    int wpi = 1;
+    while (wpi < 8 && p.n_parts > 8 * wpi * p.batch) wpi *= 2;
+    switch (wpi) {
+        case 1: return launch_merge_wpi<D, 1>(p, s);
+        case 2: return launch_merge_wpi<D, 2>(p, s);
+        case 4: return launch_merge_wpi<D, 4>(p, s);
+        default: return launch_merge_wpi<D, 8>(p, s);
     }
 }
 
@@ -761,11 +882,7 @@ bool decode_balanced_supported(int dtype, int head_dim, int group, int n_kv_head
 }
 
 cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cudaStream_t s) {
-    if (head_dim == 128)
-        decode_merge_balanced_kernel<128><<<p.batch * p.n_heads, 256, 0, s>>>(p);
-    else
-        decode_merge_balanced_kernel<64><<<p.batch * p.n_heads, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return head_dim == 128 ? launch_merge_d<128>(p, s) : launch_merge_d<64>(p, s);
 }
 
 cudaError_t launch_decode_split_mma(const DecodeParams &p, int head_dim, int group,
