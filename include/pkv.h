@@ -217,8 +217,9 @@ int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *
  * visible), else j < kv_len, reading slot req_to_token[req_pool_indices[b], j]
  * of kv head h / G.  q, o: [qo_indptr[batch], n_heads, head_dim] bf16.
  * max_q_len / max_kv_len: host-side upper bounds of q_len and kv_len (grid
- * sizing).  `ws` may be NULL.  Supported: bf16, head_dim 128 or 64,
- * G in {1, 2, 4, 8}.
+ * sizing).  `ws` may be NULL.  Supported: bf16, head_dim 128 (5th-generation
+ * tensor cores, accumulators in tensor memory) or 64 (mma.sync), G in
+ * {1, 2, 4, 8}.
  */
 int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
                       int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,

@@ -105,5 +105,8 @@ cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cu
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group,
                            cudaStream_t s);
 bool prefill_supported(int dtype, int head_dim, int group);
+// tcgen05 (TMEM) prefill for bf16 head_dim 128 (pkv_prefill_tc.cu).
+bool prefill_tc_supported(int dtype, int head_dim, int group);
+cudaError_t launch_prefill_tc(const PrefillParams &p, int group, cudaStream_t s);
 
 }  // namespace pkv

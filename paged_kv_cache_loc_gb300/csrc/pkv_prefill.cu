@@ -309,6 +309,7 @@ cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int 
                            cudaStream_t s) {
     if (!prefill_supported(dtype, head_dim, group)) return cudaErrorNotSupported;
     if (p.batch == 0 || p.max_q_len == 0) return cudaSuccess;
+    if (prefill_tc_supported(dtype, head_dim, group)) return launch_prefill_tc(p, group, s);
     return head_dim == 128 ? run_group<128>(p, group, s) : run_group<64>(p, group, s);
 }
 
