@@ -82,6 +82,22 @@ SIGNATURES = {
     "pkv_paged_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(PkvKVCache), ctypes.c_int32, _vp,
                                                 _vp, ctypes.c_int32, ctypes.c_float, _vp]),
     "pkv_last_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int64)]),
+    # include/pkv_pool.h (host page allocator)
+    "pkv_pool_create": (_vp, [ctypes.c_int32, ctypes.c_int32]),
+    "pkv_pool_destroy": (None, [_vp]),
+    "pkv_pool_page_alloc": (ctypes.c_int32, [_vp]),
+    "pkv_pool_page_free": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "pkv_pool_num_free": (ctypes.c_int32, [_vp]),
+    "pkv_pool_num_cached": (ctypes.c_int32, [_vp]),
+    "pkv_pool_refcount": (ctypes.c_int32, [_vp, ctypes.c_int32]),
+    "pkv_pool_page_hash": (ctypes.c_uint64, [_i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "pkv_pool_task_alloc": (ctypes.c_int, [_vp, ctypes.c_int64, _i32p, ctypes.c_int32, _i32p]),
+    "pkv_pool_task_free": (ctypes.c_int, [_vp, ctypes.c_int64]),
+    "pkv_pool_task_extend": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32]),
+    "pkv_pool_task_record_hashes": (ctypes.c_int, [_vp, ctypes.c_int64, _i32p, ctypes.c_int32,
+                                                   ctypes.c_int32]),
+    "pkv_pool_task_pages": (ctypes.c_int32, [_vp, ctypes.c_int64, _i32p, ctypes.c_int32]),
+    "pkv_pool_task_slots": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32, _i32p]),
     "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_version": (ctypes.c_char_p, []),
 }

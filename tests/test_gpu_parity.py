@@ -377,3 +377,50 @@ def test_balanced_decode_replays_in_a_cuda_graph():
     ref = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
                         new_lens, case.q, case.layer_id, kv_indptr=new_indptr)
     assert_close(f64(o), ref, "bf16", "balanced graph replay")
+
+
+def test_decode_on_slot_maps_from_the_page_pool():
+    """req_to_token rows produced by the host allocator after churn (shared
+    prefixes reused from the prefix cache, freed and evicted pages, decode
+    growth) drive the decode; the oracle reads the same rows."""
+    from paged_kv_cache_loc_gb300.pool import PagePool
+    ps, n_pages, H, Hk, d = 16, 256, 16, 4, 128
+    rng = np.random.Generator(np.random.PCG64(321))
+    pool = PagePool(n_pages, ps)
+    prefix = rng.integers(0, 1000, 64).tolist()
+    live = {}
+    for t in range(40):
+        prompt = prefix + rng.integers(0, 1000, int(rng.integers(1, 90))).tolist()
+        if pool.task_alloc(t, prompt)[0] != 0:
+            continue
+        pool.task_record_hashes(t, prompt)
+        live[t] = len(prompt)
+        if rng.random() < 0.5 and len(live) > 3:      # some tasks finish
+            done = list(live)[int(rng.integers(0, len(live)))]
+            pool.task_free(done)
+            del live[done]
+    for t in live:                                      # one decode step each
+        assert pool.task_extend(t, live[t]) == 0
+        live[t] += 1
+    tids = sorted(live)
+    B = len(tids)
+    seq = np.array([live[t] for t in tids], np.int32)
+    max_ctx = int(seq.max())
+    r2t = np.zeros((B, max_ctx), np.int32)
+    for b, t in enumerate(tids):
+        r2t[b, :seq[b]] = pool.task_slots(t, int(seq[b]))
+    size = n_pages * ps
+    kb = W.to_bf16_bits(rng.standard_normal((2, size, Hk, d), dtype=np.float32))
+    vb = W.to_bf16_bits(rng.standard_normal((2, size, Hk, d), dtype=np.float32))
+    q = W.to_bf16_bits(rng.standard_normal((B, H, d), dtype=np.float32))
+    rpi = np.arange(B, dtype=np.int32)
+    kvi = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
+    dev = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+                     else torch.from_numpy(a)).cuda()
+    cache = pkv.KVCache(k_buffer=dev(kb), v_buffer=dev(vb), req_to_token=dev(r2t),
+                        req_pool_indices=dev(rpi), seq_lens=dev(seq), kv_indptr=dev(kvi),
+                        max_len=max_ctx)
+    o = pkv.paged_decode(cache, 1, dev(q), workspace=pkv.Workspace(B, H, d, 64))
+    no_device_error()
+    ref = oracle.decode(kb, vb, r2t, rpi, seq, q, 1, kv_indptr=kvi)
+    assert_close(f64(o), ref, "bf16", "pool slot maps")
