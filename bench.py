@@ -51,7 +51,47 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the prefill / long-context / e2e / cpu legs")
     ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "kvwrite"],
+                    help="run a few untimed calls of one kernel's case (for ncu) and exit")
     return ap.parse_args()
+
+
+def run_profile_case(which: str) -> None:
+    """A few untimed calls of one workload, sized for an ncu capture (a few GB
+    on the device at most): decode = the batched decode (98,304-slot pool),
+    long = B=1 at 32,768 tokens, prefill = 4 ragged-prefill requests,
+    kvwrite = the ragged prefill's cache write (17,418 tokens)."""
+    import torch
+    import paged_kv_cache_loc_gb300 as pkv
+    from paged_kv_cache_loc_gb300 import build
+    from paged_kv_cache_loc_gb300 import workloads as W
+    build.build()
+    torch.cuda.set_device(0)
+    if which in ("decode", "long"):
+        case = W.batched_decode(size=98304) if which == "decode" else W.long_decode(32768)
+        cache, q, kn, vn = W.upload(case)
+        pkv.kv_write(cache, case.layer_id, kn, vn)
+        ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024)
+        o = torch.empty_like(q)
+        for _ in range(3):
+            pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws)
+    elif which == "prefill":
+        case = W.ragged_prefill(batch=4, size=32768)
+        cache, q, kn, vn = W.upload(case)
+        pkv.kv_write(cache, case.layer_id, kn, vn)
+        o = torch.empty_like(q)
+        for _ in range(2):
+            pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o)
+    else:
+        case = W.ragged_prefill()
+        cache, q, kn, vn = W.upload(case)
+        for _ in range(3):
+            pkv.kv_write(cache, case.layer_id, kn, vn)
+    torch.cuda.synchronize()
+    st, detail = pkv.last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error word set ({detail})")
+    print(f"profile case {which}: done")
 
 
 # ---------------------------------------------------------------------------
@@ -144,9 +184,9 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def profile_traffic(name: str, source: str):
+def profile_traffic(name: str, *sources: str):
     """DRAM bytes per launch from a committed ncu summary, or None if the kernel
-    source changed since it was captured (the summary records its sha256)."""
+    sources changed since it was captured (the summary records their sha256)."""
     path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path).read()
@@ -157,8 +197,10 @@ def profile_traffic(name: str, source: str):
         if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "paged_kv_cache_loc_gb300", "csrc", source)
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for source in sources:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_loc_gb300", "csrc", source), "rb").read())
+    digest = h.hexdigest()
     if fields.get("source_sha256") != digest or "traffic_bytes_per_launch" not in fields:
         return None
     return float(fields["traffic_bytes_per_launch"])
@@ -330,7 +372,8 @@ def run_pkv(args):
         "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
         "frac": round(achieved / peaks["hbm_gbs"], 4),
         "peak_source": peaks["hbm_source"],
-        "traffic": profile_traffic("decode_batched_b32_traffic.txt", "pkv_decode.cu"),
+        "traffic": profile_traffic("decode_split_batched_b32.md", "pkv_decode.cu", "pkv_decode_mma.cu"),
+        "traffic_note": "split + merge DRAM bytes of one call from the committed ncu summary",
         "algorithmic_bytes_per_launch": b_dec,
         "ms_per_launch": round(ms_decode, 5),
     }
@@ -551,7 +594,9 @@ def run_reference(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_pkv(args)
