@@ -435,32 +435,51 @@ decode_mma_allheads_kernel(const DecodeParams p) {
             __syncthreads();
             const int nst = (len + C::kTS - 1) / C::kTS;
             const uint32_t first = issued;   // global index of this piece's stage 0
-            // Warp 0 fills stage k: every token row of K and of V is one bulk
-            // copy of all kv heads; rows past the piece repeat the first
-            // token's row so that the stage always holds finite data.
+            // Stage k: the K rows go through the bulk-copy (TMA) engine, one
+            // copy per token row of all kv heads, counted on the stage's
+            // mbarrier (issued by warp 0); the V rows go through the load/store
+            // path as 16-byte cp.async chunks from every thread, one commit
+            // group per stage.  Splitting the bytes between the two copy
+            // engines keeps either from capping the stream.  Rows past the
+            // piece repeat the first token's row so the stage holds finite data.
             auto issue = [&](int k) {
                 const uint32_t g = first + k;
                 const int st = g % C::kStages;
-                const uint32_t bar = smem_u32(bars + st);
-                if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(C::kStageBytes - 2 * C::kTS * 16));
-                __syncwarp();
                 bf16 *dst0 = ring + st * C::kStageElems;
-                for (int i = lane; i < 2 * C::kTS; i += 32) {
-                    const int kv = i / C::kTS, t = i - kv * C::kTS;
-                    const int tok = k * C::kTS + t;
-                    const int slot = slots[tok < len ? tok : 0];
-                    bulk_g2s(smem_u32(dst0 + kv * C::kPartElems + t * C::kPitch),
-                             (kv ? vbase : kbase) + slot * slot_stride, C::kRowBytes, bar);
+                if (warp == 0) {
+                    const uint32_t bar = smem_u32(bars + st);
+                    if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(C::kTS * C::kRowBytes));
+                    __syncwarp();
+                    for (int t = lane; t < C::kTS; t += 32) {
+                        const int tok = k * C::kTS + t;
+                        bulk_g2s(smem_u32(dst0 + t * C::kPitch),
+                                 kbase + slots[tok < len ? tok : 0] * slot_stride, C::kRowBytes, bar);
+                    }
                 }
+                constexpr int kVChunks = C::kRowBytes / 16;   // per token row
+                bf16 *vdst = dst0 + C::kPartElems;
+#pragma unroll
+                for (int i = tid; i < C::kTS * kVChunks; i += NT) {
+                    const int t = i / kVChunks, c = i - t * kVChunks;
+                    const int tok = k * C::kTS + t;
+                    cp_async16(vdst + t * C::kPitch + c * 8,
+                               vbase + slots[tok < len ? tok : 0] * slot_stride + c * 8);
+                }
+                cp_async_commit();
             };
-            if (warp == 0 && !s_abort) {
-                for (int k = 0; k < C::kStages - 1 && k < nst; ++k) issue(k);
+            if (!s_abort) {
+                for (int k = 0; k < C::kStages - 1; ++k) {
+                    if (k < nst) issue(k);
+                    else cp_async_commit();
+                }
             }
             issued += nst;
             for (int k = 0; k < nst; ++k) {
-                __syncthreads();   // stage k-1 is consumed: its buffer may be refilled
+                cp_async_wait<C::kStages - 2>();   // this thread's V chunks of stage k
+                __syncthreads();   // stage k-1 is consumed; everyone's V of stage k landed
                 if (s_abort) continue;   // CTA-uniform after the barrier
-                if (warp == 0 && k + C::kStages - 1 < nst) issue(k + C::kStages - 1);
+                if (k + C::kStages - 1 < nst) issue(k + C::kStages - 1);
+                else cp_async_commit();
                 const uint32_t g = first + k;
                 const bool ok = __all_sync(0xffffffffu,
                                            mbar_wait(smem_u32(bars + g % C::kStages), (g / C::kStages) & 1));
@@ -523,6 +542,7 @@ decode_mma_allheads_kernel(const DecodeParams p) {
                     mma16816(o_acc[mt], a, pb0, pb1);
                 }
             }
+            cp_async_wait<0>();
             __syncthreads();   // ring and slots are free for the next piece / the combine
         }
 
