@@ -460,25 +460,33 @@ def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
 
 
 def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
-    """B=1 decode at 32768 tokens of context (split-K across the SMs)."""
-    case = W.long_decode(32768)
-    cache, q, kn, vn = W.upload(case, dev)
-    pkv.kv_write(cache, case.layer_id, kn, vn)
-    ws = pkv.Workspace(1, case.n_heads, case.head_dim, 1024, device=dev)
-    o = torch.empty_like(q)
-    plan_chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
-    with torch.cuda.stream(stream):
-        ms, _ = timed(torch, stream,
-                      lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
-                                               stream=stream), 100, 10, flush)
-    t = statistics.median(ms)
-    b = decode_bytes(case)
-    gbs = b / (t * 1e-3) / 1e9
-    return {"context": 32768, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
-            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
-            "decode_plan": (f"balanced: {n_splits} CTAs" if plan_chunk == 0
-                            else f"chunked: {plan_chunk}-token splits"),
-            "algorithmic_bytes": b}
+    """B=1 decode over the long-context sweep (1K-32K tokens, split-K across
+    the SMs); the 32,768-token point is the headline."""
+    sweep = []
+    for ctx in W.LONG_CONTEXTS:
+        case = W.long_decode(ctx)
+        cache, q, kn, vn = W.upload(case, dev)
+        pkv.kv_write(cache, case.layer_id, kn, vn)
+        ws = pkv.Workspace(1, case.n_heads, case.head_dim, 1024, device=dev)
+        o = torch.empty_like(q)
+        plan_chunk, n_splits = pkv.decode_plan(cache, case.n_heads, ws)
+        with torch.cuda.stream(stream):
+            ms, _ = timed(torch, stream,
+                          lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
+                                                   stream=stream), 100, 10, flush)
+        t = statistics.median(ms)
+        b = decode_bytes(case)
+        gbs = b / (t * 1e-3) / 1e9
+        sweep.append({"context": ctx, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
+                      "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                      "decode_plan": (f"balanced: {n_splits} CTAs" if plan_chunk == 0
+                                      else f"chunked: {plan_chunk}-token splits"),
+                      "algorithmic_bytes": b})
+        del cache, q, kn, vn, ws, o
+    out = dict(sweep[-1])
+    out["sweep"] = [{k: s[k] for k in ("context", "us_per_decode", "kv_gbs", "frac_of_hbm_peak")}
+                    for s in sweep]
+    return out
 
 
 def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):

@@ -90,7 +90,8 @@ int ws_check(const pkv_workspace *ws) {
 //  balanced: chosen when the caller asked for the automatic plan, passed
 //    kv_indptr, the shape has a balanced kernel and the workspace holds
 //    (n_parts + batch) * n_heads partial rows.  n_parts CTAs (one per SM, or
-//    fewer for small batches) share all tokens of the batch equally.
+//    fewer when the batch holds less than ~32 tokens per SM) share all tokens
+//    of the batch equally.
 //  chunked: each entry's context is cut into chunks; about four CTAs per SM
 //    if every context were max_len long, 64..2048 tokens in steps of 32, never
 //    more splits than the workspace holds (one split without a workspace).
@@ -116,7 +117,7 @@ int make_plan(const pkv_kvcache *c, int32_t n_heads, int sms, const pkv_workspac
     const bool have_ws = ws_check(ws) == PKV_OK;
     if (chunk_req == 0 && c->kv_indptr && have_ws &&
         pkv::decode_balanced_supported(c->dtype, c->head_dim, group, c->n_kv_heads)) {
-        int64_t parts = (max_len * batch + 127) / 128;   // at least ~128 tokens per CTA
+        int64_t parts = (max_len * batch + 31) / 32;   // at least ~32 tokens (2 stages) per CTA
         const int64_t cap = sms > 0 ? sms : 1;
         if (parts > cap) parts = cap;
         if (parts < 1) parts = 1;

@@ -364,10 +364,322 @@ struct AllHeadsCfg {
     static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0, "bulk copies move 16-byte units");
 };
 
+// One 16-token block of one kv head: scores S^T = K Q^T (16 tokens x 8
+// heads), base-2 online softmax over the `valid` leading tokens (the rest
+// score -inf), O^T += V^T P^T.  kt / vt point at the block's first row in
+// shared memory (row pitch `pitch` elements).  m*/l* are the running max
+// and sum of the two heads (columns) this lane holds.
+template <int D>
+__device__ __forceinline__ void block_math(const __nv_bfloat16 *kt, const __nv_bfloat16 *vt,
+                                           int pitch, int valid, int lane, float scale_log2,
+                                           const uint32_t (&qb)[D / 16][2], float (&o_acc)[D / 16][4],
+                                           float &m0, float &m1, float &l0, float &l1) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, kt + (lane & 15) * pitch + (2 * ks + (lane >> 4)) * 8);
+        mma16816(s, a, qb[ks][0], qb[ks][1]);
+    }
+    const int tA = lane >> 2, tB = tA + 8;
+    s[0] = tA < valid ? s[0] * scale_log2 : -INFINITY;
+    s[1] = tA < valid ? s[1] * scale_log2 : -INFINITY;
+    s[2] = tB < valid ? s[2] * scale_log2 : -INFINITY;
+    s[3] = tB < valid ? s[3] * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+    const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+    l0 = l0 * al0 + p0 + p2;
+    l1 = l1 * al1 + p1 + p3;
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+            o_acc[i][0] *= al0;
+            o_acc[i][1] *= al1;
+            o_acc[i][2] *= al0;
+            o_acc[i][3] *= al1;
+        }
+    }
+    const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+    const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, vt + ((lane & 7) + ((lane >> 4) << 3)) * pitch + (2 * mt + ((lane >> 3) & 1)) * 8);
+        mma16816(o_acc[mt], a, pb0, pb1);
+    }
+}
+
 // First CTA index of the balanced partition whose range holds token t.
 __device__ __forceinline__ int part_of(long long t, long long T, int P) {
     const long long c = ((t + 1) * P - 1) / T;
     return static_cast<int>(c < P - 1 ? c : P - 1);
+}
+
+// Balanced-mode CTA c with one warp per kv head (8 kv heads), when its range
+// [t0, t1) holds at most kMaxPieces entry pieces and their slots fit the slot
+// array after rounding each piece up to whole 16-token stages.  Then:
+//  - the pieces come from the metadata the caller read in one round trip
+//    (ip: kv_indptr[KPT i .. KPT i + KPT], rq / sq: req_pool_indices /
+//    seq_lens of this thread's KPT entries) and a block-wide scan;
+//  - all slot indices are staged at once, each piece padded to a multiple
+//    of 16 by repeating its last slot, so stage k is simply slots
+//    [16k, 16k + 16) and the copy ring runs across piece boundaries without
+//    draining;
+//  - each warp finishes a piece straight from its registers (it owns its kv
+//    head, so no cross-warp combine): o for a whole entry, else the partial
+//    row (c + b).
+// Returns false (having done nothing but read) when the range does not
+// fit; the caller then takes the piece-by-piece path.
+constexpr int kMaxPieces = 64;
+
+template <int D, int G, int KPT>
+__device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long long t0, long long t1,
+                                              int n_cap, const int (&ip)[KPT + 1], const int (&rq)[KPT],
+                                              const int (&sq)[KPT], int *slots, uint64_t *bars,
+                                              __nv_bfloat16 *ring) {
+    using C = AllHeadsCfg<D, 8>;
+    using bf16 = __nv_bfloat16;
+    constexpr int NW = C::kWarpsAH, NT = C::kNTAH, S = C::kStages;
+    static_assert(C::kTS == 16, "one 16-token block per warp and stage");
+    __shared__ int s_scan[NW][2];
+    __shared__ int s_b[kMaxPieces], s_r[kMaxPieces], s_s0[kMaxPieces], s_len[kMaxPieces],
+        s_off[kMaxPieces], s_direct[kMaxPieces];
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e0 = tid * KPT;
+
+    // this thread's pieces: non-empty, valid entries overlapping [t0, t1)
+    int cnt = 0, pad = 0;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const long long lo = ip[k], hi = ip[k + 1];
+        if (e0 + k < p.batch && hi > t0 && lo < t1 && hi > lo) {
+            const bool ok = hi - lo == sq[k] && hi - lo <= n_cap && lo >= 0 &&
+                            static_cast<unsigned>(rq[k]) < static_cast<unsigned>(p.num_reqs);
+            if (ok) {
+                ++cnt;
+                pad += (static_cast<int>(min(hi, t1) - max(lo, t0)) + 15) & ~15;
+            }
+        }
+    }
+    // block-wide exclusive scan of (pieces, padded tokens) in entry order
+    int ic = cnt, ipd = pad;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ic, off), b = __shfl_up_sync(0xffffffffu, ipd, off);
+        if (lane >= off) {
+            ic += a;
+            ipd += b;
+        }
+    }
+    if (lane == 31) {
+        s_scan[warp][0] = ic;
+        s_scan[warp][1] = ipd;
+    }
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+    int n_pieces = 0, total = 0, cbase = ic - cnt, pbase = ipd - pad;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) {
+            cbase += s_scan[w][0];
+            pbase += s_scan[w][1];
+        }
+        n_pieces += s_scan[w][0];
+        total += s_scan[w][1];
+    }
+    if (n_pieces > kMaxPieces || total > kDecodeMaxChunk) return false;   // CTA-uniform
+
+    // the piece table, and errors for overlapping entries that fail validation
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const long long lo = ip[k], hi = ip[k + 1];
+        if (e0 + k < p.batch && hi > t0 && lo < t1 && hi > lo) {
+            const bool ok = hi - lo == sq[k] && hi - lo <= n_cap && lo >= 0 &&
+                            static_cast<unsigned>(rq[k]) < static_cast<unsigned>(p.num_reqs);
+            if (!ok) {
+                record_error(p.err, hi - lo);
+                continue;
+            }
+            const int len = static_cast<int>(min(hi, t1) - max(lo, t0));
+            s_b[cbase] = e0 + k;
+            s_r[cbase] = rq[k];
+            s_s0[cbase] = static_cast<int>(max(lo, t0) - lo);
+            s_len[cbase] = len;
+            s_off[cbase] = pbase;
+            s_direct[cbase] = lo >= t0 && hi <= t1;
+            ++cbase;
+            pbase += (len + 15) & ~15;
+        }
+    }
+    __syncthreads();
+    if (n_pieces == 0) return true;
+
+    const int hw = warp;   // this warp's kv head
+    auto load_q = [&](int pc, uint32_t (&qr)[D / 16][2]) {
+        const int h = lane >> 2;
+        const bf16 *qrow = static_cast<const bf16 *>(p.q) +
+                           (static_cast<int64_t>(s_b[pc]) * p.n_heads + hw * G + (h < G ? h : 0)) * D +
+                           2 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qr[ks][0] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16) : 0u;
+            qr[ks][1] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8) : 0u;
+        }
+    };
+    uint32_t qb[D / 16][2], qn[D / 16][2];
+    load_q(0, qb);
+    if (n_pieces > 1) load_q(1, qn);
+
+    // stage every slot index (padding rows repeat the piece's last slot)
+    for (int j = tid; j < total; j += NT) {
+        int a = 0, z = n_pieces - 1;   // last piece with s_off <= j
+        while (a < z) {
+            const int mid = (a + z + 1) >> 1;
+            if (s_off[mid] <= j) a = mid; else z = mid - 1;
+        }
+        const int pos = min(j - s_off[a], s_len[a] - 1);
+        int sl = __ldg(p.req_to_token + static_cast<int64_t>(s_r[a]) * p.max_ctx_len + s_s0[a] + pos);
+        if (static_cast<unsigned long long>(static_cast<long long>(sl)) >=
+            static_cast<unsigned long long>(p.size)) {
+            record_error(p.err, sl);
+            sl = 0;
+        }
+        slots[j] = sl;
+    }
+    __syncthreads();
+
+    const int64_t slot_stride = static_cast<int64_t>(8) * D;
+    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + p.layer_row0 * slot_stride;
+    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + p.layer_row0 * slot_stride;
+    const int nst = total / 16;
+    // stage k: K rows by bulk copy (warp 0, one per token, on the stage's
+    // mbarrier), V rows as 16-byte cp.async chunks from every thread (one
+    // commit group per stage)
+    auto issue = [&](int k) {
+        const int st = k % S;
+        bf16 *dst0 = ring + st * C::kStageElems;
+        const int *sl = slots + k * 16;
+        if (warp == 0) {
+            const uint32_t bar = smem_u32(bars + st);
+            if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(16 * C::kRowBytes));
+            __syncwarp();
+            if (lane < 16)
+                bulk_g2s(smem_u32(dst0 + lane * C::kPitch), kbase + sl[lane] * slot_stride, C::kRowBytes, bar);
+        }
+        constexpr int kVChunks = C::kRowBytes / 16;
+        bf16 *vdst = dst0 + C::kPartElems;
+#pragma unroll
+        for (int i = tid; i < 16 * kVChunks; i += NT) {
+            const int t = i / kVChunks, ch = i - t * kVChunks;
+            cp_async16(vdst + t * C::kPitch + ch * 8, vbase + sl[t] * slot_stride + ch * 8);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        if (k < nst) issue(k);
+        else cp_async_commit();
+    }
+
+    float o_acc[D / 16][4];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int pc = 0;                                        // piece being consumed
+    int pend = (s_off[0] + ((s_len[0] + 15) & ~15)) >> 4;   // its end stage
+    for (int k = 0; k < nst; ++k) {
+        cp_async_wait<S - 2>();   // this thread's V chunks of stage k
+        __syncthreads();          // stage k-1 is consumed; everyone's V of stage k landed
+        if (s_abort) break;       // CTA-uniform after the barrier
+        if (k + S - 1 < nst) issue(k + S - 1);
+        else cp_async_commit();
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bars + k % S), (k / S) & 1));
+        if (!ok) {
+            if (lane == 0) {
+                record_error(p.err, -1000 - k);
+                s_abort = 1;
+            }
+            continue;
+        }
+        const bf16 *kt = ring + (k % S) * C::kStageElems + hw * D;
+        block_math<D>(kt, kt + C::kPartElems, C::kPitch, s_len[pc] - (k * 16 - s_off[pc]), lane,
+                      p.scale_log2, qb, o_acc, m0, m1, l0, l1);
+        if (k + 1 < pend) continue;
+
+        // piece pc is complete: normalise and write it from registers
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int b = s_b[pc];
+        const int h0 = 2 * (lane & 3), h1 = h0 + 1;
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+        if (s_direct[pc]) {
+            bf16 *o = static_cast<bf16 *>(p.o) + (static_cast<int64_t>(b) * p.n_heads + hw * G) * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d = mt * 16 + (lane >> 2);
+                if (h0 < G) {
+                    o[h0 * D + d] = __float2bfloat16_rn(o_acc[mt][0] * i0);
+                    o[h0 * D + d + 8] = __float2bfloat16_rn(o_acc[mt][2] * i0);
+                }
+                if (h1 < G) {
+                    o[h1 * D + d] = __float2bfloat16_rn(o_acc[mt][1] * i1);
+                    o[h1 * D + d + 8] = __float2bfloat16_rn(o_acc[mt][3] * i1);
+                }
+            }
+        } else {
+            const int64_t row = (static_cast<int64_t>(c) + b) * p.n_heads + hw * G;
+            float *op = p.o_part + row * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d = mt * 16 + (lane >> 2);
+                if (h0 < G) {
+                    op[h0 * D + d] = o_acc[mt][0] * i0;
+                    op[h0 * D + d + 8] = o_acc[mt][2] * i0;
+                }
+                if (h1 < G) {
+                    op[h1 * D + d] = o_acc[mt][1] * i1;
+                    op[h1 * D + d + 8] = o_acc[mt][3] * i1;
+                }
+            }
+            if (lane < 4) {
+                if (h0 < G) {
+                    p.ml_part[(row + h0) * 2] = m0;
+                    p.ml_part[(row + h0) * 2 + 1] = l0;
+                }
+                if (h1 < G) {
+                    p.ml_part[(row + h1) * 2] = m1;
+                    p.ml_part[(row + h1) * 2 + 1] = l1;
+                }
+            }
+        }
+        if (++pc == n_pieces) break;
+        pend = (s_off[pc] + ((s_len[pc] + 15) & ~15)) >> 4;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+            o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+            qb[i][0] = qn[i][0];
+            qb[i][1] = qn[i][1];
+        }
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+        if (pc + 1 < n_pieces) load_q(pc + 1, qn);
+    }
+    cp_async_wait<0>();
+    return true;
 }
 
 template <int D, int G, int HK>
@@ -493,54 +805,10 @@ decode_mma_allheads_kernel(const DecodeParams p) {
 
                 const int valid = len - (k * C::kTS + blk * kBlk);
                 if (valid <= 0) continue;   // warp-uniform
-                const bf16 *kt = ring + ((first + k) % C::kStages) * C::kStageElems + hw * D;
-                const bf16 *vt = kt + C::kPartElems;
-                const int r0 = blk * kBlk;
-
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t a[4];
-                    ldsm_x4(a, kt + (r0 + (lane & 15)) * C::kPitch + (2 * ks + (lane >> 4)) * 8);
-                    mma16816(s, a, qb[ks][0], qb[ks][1]);
-                }
-                const int tA = lane >> 2, tB = tA + 8;
-                s[0] = tA < valid ? s[0] * p.scale_log2 : -INFINITY;
-                s[1] = tA < valid ? s[1] * p.scale_log2 : -INFINITY;
-                s[2] = tB < valid ? s[2] * p.scale_log2 : -INFINITY;
-                s[3] = tB < valid ? s[3] * p.scale_log2 : -INFINITY;
-                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-                m0 = mn0;
-                m1 = mn1;
-                const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-                const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
-                l0 = l0 * al0 + p0 + p2;
-                l1 = l1 * al1 + p1 + p3;
-                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-                    for (int i = 0; i < D / 16; ++i) {
-                        o_acc[i][0] *= al0;
-                        o_acc[i][1] *= al1;
-                        o_acc[i][2] *= al0;
-                        o_acc[i][3] *= al1;
-                    }
-                }
-                const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-                const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
-#pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_t(a, vt + (r0 + (lane & 7) + ((lane >> 4) << 3)) * C::kPitch +
-                                     (2 * mt + ((lane >> 3) & 1)) * 8);
-                    mma16816(o_acc[mt], a, pb0, pb1);
-                }
+                const bf16 *kt = ring + ((first + k) % C::kStages) * C::kStageElems +
+                                 blk * kBlk * C::kPitch + hw * D;
+                block_math<D>(kt, kt + C::kPartElems, C::kPitch, valid, lane, p.scale_log2, qb, o_acc,
+                              m0, m1, l0, l1);
             }
             cp_async_wait<0>();
             __syncthreads();   // ring and slots are free for the next piece / the combine
@@ -635,13 +903,34 @@ decode_mma_allheads_kernel(const DecodeParams p) {
     }
 
     // balanced partition of [0, T)
+    const int c = blockIdx.x;
+    // With one warp per kv head (HK == NW) and at most KPT * NT entries, the
+    // entries' metadata comes in one round trip together with T: thread i
+    // holds entries [KPT i, KPT i + KPT).
+    constexpr int KPT = 4;
+    constexpr bool kFast = HK == NW;
+    const bool fast_batch = kFast && p.batch <= KPT * NT;
+    const int e0 = tid * KPT;
+    int ip[KPT + 1], rq[KPT], sq[KPT];
+#pragma unroll
+    for (int k = 0; k <= KPT; ++k) ip[k] = fast_batch && e0 + k <= p.batch ? __ldg(p.kv_indptr + e0 + k) : 0;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        rq[k] = fast_batch && e0 + k < p.batch ? __ldg(p.req_pool_indices + e0 + k) : 0;
+        sq[k] = fast_batch && e0 + k < p.batch ? __ldg(p.seq_lens + e0 + k) : 0;
+    }
     const long long T = __ldg(p.kv_indptr + p.batch);
     if (T <= 0) return;
     const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
-    const int c = blockIdx.x;
     if (c >= P) return;
     long long t0 = T * c / P;
     const long long t1 = T * (c + 1) / P;
+
+    if constexpr (kFast) {
+        if (fast_batch && stream_pieces<D, G, KPT>(p, c, t0, t1, n_cap, ip, rq, sq, slots, bars, ring))
+            return;
+    }
+
     int lo_b = 0, hi_b = p.batch - 1;   // first entry whose range ends after t0
     while (lo_b < hi_b) {
         const int mid = (lo_b + hi_b) >> 1;
@@ -699,14 +988,16 @@ cudaError_t run_hk(const DecodeParams &p, cudaStream_t s) {
 
 // Merge of the balanced mode.  Entry b's pieces are partial rows c + b for c
 // in [part_of(lo), part_of(hi - 1)] (a single piece was written to o by the
-// split kernel).  WPI warps merge one (entry, head): warp `sub` takes pieces
-// sub, sub + WPI, ... in batches of 32 — lane k loads (m, l) of the batch's
-// k-th piece, the batch is folded into a running (M, L, acc) with one
-// rescale, and every lane keeps float4 columns of the output with 8 piece
-// loads in flight.  WPI > 1 warps are combined through shared memory.
+// split kernel).  WPI warps merge one (entry, head); warp `sub` takes pieces
+// sub, sub + WPI, ... kBatch at a time, loading each piece's (m, l) (the
+// same address in every lane) and its float4 columns together, so one
+// round trip to L2 brings a whole batch.  A batch folds into the warp's
+// running (M, L, acc) with one rescale; WPI > 1 warps then combine through
+// shared memory.
 template <int D, int WPI>
-__global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const DecodeParams p) {
-    constexpr int NW = 8, IPC = NW / WPI, kCols = D / 4;
+__global__ void __launch_bounds__(WPI > 8 ? 32 * WPI : 256) decode_merge_balanced_kernel(const DecodeParams p) {
+    constexpr int NW = WPI > 8 ? WPI : 8, IPC = NW / WPI, kCols = D / 4;
+    constexpr int kBatch = WPI == 16 ? 10 : 8;
     __shared__ float red_ml[NW][2];
     __shared__ float4 red_o[NW][kCols];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -741,54 +1032,41 @@ __global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const Decode
             asm volatile("griddepcontrol.wait;\n" ::: "memory");
             if (merge) {
                 const int mine = np > sub ? (np - sub + WPI - 1) / WPI : 0;   // pieces of this warp
-                for (int base = 0; base < mine; base += 32) {
-                    const int k = base + lane;
-                    float m = -INFINITY, l = 0.f;
-                    if (k < mine) {
-                        const int64_t rr = row0 + static_cast<int64_t>(sub + k * WPI) * p.n_heads;
-                        m = __ldcg(p.ml_part + rr * 2);
-                        l = __ldcg(p.ml_part + rr * 2 + 1);
-                    }
-                    float bm = m;
+                for (int base = 0; base < mine; base += kBatch) {
+                    float m[kBatch], l[kBatch];
+                    float4 x[kBatch];
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1)
-                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-                    const float nM = fmaxf(M, bm);
+                    for (int u = 0; u < kBatch; ++u) {
+                        m[u] = -INFINITY;
+                        l[u] = 0.f;
+                        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (base + u < mine) {
+                            const int64_t rr = row0 + static_cast<int64_t>(sub + (base + u) * WPI) * p.n_heads;
+                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ml_part) + rr);
+                            m[u] = ml.x;
+                            l[u] = ml.y;
+                            if (lane < kCols) x[u] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + rr * D) + lane);
+                        }
+                    }
+                    float nM = M;
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) nM = fmaxf(nM, m[u]);
                     const float sc = exp2f(M - nM);   // M = -inf on the first batch: 0
                     acc.x *= sc;
                     acc.y *= sc;
                     acc.z *= sc;
                     acc.w *= sc;
-                    const float w = k < mine ? l * exp2f(m - nM) : 0.f;
-                    float ws = w;
+                    L *= sc;
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
-                    L = L * sc + ws;
-                    M = nM;
-                    const int cnt = min(32, mine - base);
-                    for (int k0 = 0; k0 < cnt; k0 += 8) {
-                        float4 x[8];
-                        float wk[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            wk[u] = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
-                            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (k0 + u < cnt && lane < kCols) {
-                                const int64_t rr =
-                                    row0 + static_cast<int64_t>(sub + (base + k0 + u) * WPI) * p.n_heads;
-                                x[u] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + rr * D) + lane);
-                            }
-                        }
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            if (k0 + u < cnt) {
-                                acc.x = fmaf(wk[u], x[u].x, acc.x);
-                                acc.y = fmaf(wk[u], x[u].y, acc.y);
-                                acc.z = fmaf(wk[u], x[u].z, acc.z);
-                                acc.w = fmaf(wk[u], x[u].w, acc.w);
-                            }
-                        }
+                    for (int u = 0; u < kBatch; ++u) {
+                        const float w = base + u < mine ? l[u] * exp2f(m[u] - nM) : 0.f;
+                        L += w;
+                        acc.x = fmaf(w, x[u].x, acc.x);
+                        acc.y = fmaf(w, x[u].y, acc.y);
+                        acc.z = fmaf(w, x[u].z, acc.z);
+                        acc.w = fmaf(w, x[u].w, acc.w);
                     }
+                    M = nM;
                 }
             }
         }
@@ -808,7 +1086,7 @@ __global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const Decode
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int u = 0; u < WPI; ++u) {
-                const float sc = exp2f(red_ml[warp + u][0] - MM);
+                const float sc = exp2f(red_ml[warp + u][0] - MM);   // a warp without pieces: 0
                 LL += red_ml[warp + u][1] * sc;
                 if (lane < kCols) {
                     const float4 t = red_o[warp + u][lane];
@@ -833,10 +1111,10 @@ __global__ void __launch_bounds__(256) decode_merge_balanced_kernel(const Decode
 template <int D, int WPI>
 cudaError_t launch_merge_wpi(const DecodeParams &p, cudaStream_t s) {
     const int items = p.batch * p.n_heads;
-    const int ipc = 8 / WPI;
+    const int ipc = WPI > 8 ? 1 : 8 / WPI;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((items + ipc - 1) / ipc);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(WPI > 8 ? 32 * WPI : 256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -849,15 +1127,17 @@ cudaError_t launch_merge_wpi(const DecodeParams &p, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_merge_d(const DecodeParams &p, cudaStream_t s) {
-    // pieces per entry are about n_parts / batch + 1: give an (entry, head)
-    // more warps when there are many
+    // an entry has about (n_parts + batch) / batch pieces: up to 16 warps per
+    // entry, each loading its pieces in one or two batches
+    const int64_t per_entry = (static_cast<int64_t>(p.n_parts) + p.batch) / (p.batch > 0 ? p.batch : 1);
     int wpi = 1;
-    while (wpi < 8 && p.n_parts > 8 * wpi * p.batch) wpi *= 2;
+    while (wpi < 16 && per_entry > 8 * wpi) wpi *= 2;
     switch (wpi) {
         case 1: return launch_merge_wpi<D, 1>(p, s);
         case 2: return launch_merge_wpi<D, 2>(p, s);
         case 4: return launch_merge_wpi<D, 4>(p, s);
-        default: return launch_merge_wpi<D, 8>(p, s);
+        case 8: return launch_merge_wpi<D, 8>(p, s);
+        default: return launch_merge_wpi<D, 16>(p, s);
     }
 }
 

@@ -177,6 +177,7 @@ def test_ragged_prefill_full_size_sampled():
 
 @pytest.mark.parametrize("dtype,heads,hk,d", [
     ("bf16", 8, 8, 128), ("bf16", 16, 8, 128), ("bf16", 32, 4, 128), ("bf16", 16, 4, 64),
+    ("bf16", 64, 8, 64),
     ("f32", 32, 8, 128), ("f32", 8, 1, 64), ("f32", 4, 2, 64),
 ])
 def test_decode_variants_and_ragged_lengths(dtype, heads, hk, d):
@@ -257,19 +258,25 @@ def test_kv_write_duplicate_free_scatter_leaves_other_rows():
     check_pool_bit_exact(cache, case)
 
 
-def test_device_data_errors_are_reported_not_faulted():
+@pytest.mark.parametrize("hk,indptr", [(2, False), (2, True), (8, True)])
+def test_device_data_errors_are_reported_not_faulted(hk, indptr):
+    """Bad device data is recorded in the error word, never faulted, on the
+    chunked plan and on the balanced plan (with 8 kv heads, its staged-slot
+    pass)."""
     case = W.make_case("bad", mode="decode", dtype="bf16", n_layers=2, layer_id=1, size=512,
-                       n_heads=8, n_kv_heads=2, head_dim=128, kv_lens=[20, 40], seed=3)
+                       n_heads=8, n_kv_heads=hk, head_dim=128, kv_lens=[20, 40], seed=3)
     cache, q = prepare(case)
     no_device_error()
     ws = ws_for(case)
+    kvi = cache.kv_indptr if indptr else None
     # a slot outside the pool in req_to_token
     r2t = case.req_to_token.copy()
     r2t[case.req_pool_indices[1], 7] = case.size + 5
     bad = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
                       req_to_token=torch.from_numpy(r2t).cuda(),
                       req_pool_indices=cache.req_pool_indices, seq_lens=cache.seq_lens,
-                      max_len=case.max_len)
+                      kv_indptr=kvi, max_len=case.max_len)
+    assert (pkv.decode_plan(bad, case.n_heads, ws)[0] == 0) == indptr
     pkv.paged_decode(bad, 1, q, workspace=ws)
     st, detail = pkv.last_device_error()
     assert st == _lib.PKV_ERR_INDEX and detail == case.size + 5
@@ -278,17 +285,74 @@ def test_device_data_errors_are_reported_not_faulted():
     bad.req_pool_indices = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
     pkv.paged_decode(bad, 1, q, workspace=ws)
     assert pkv.last_device_error()[0] == _lib.PKV_ERR_INDEX
+    if indptr:
+        # kv_indptr that disagrees with seq_lens
+        bad.req_pool_indices = cache.req_pool_indices
+        bad.seq_lens = torch.tensor([20, 41], dtype=torch.int32, device="cuda")
+        pkv.paged_decode(bad, 1, q, workspace=ws)
+        assert pkv.last_device_error()[0] == _lib.PKV_ERR_INDEX
     # a write location outside the pool
     wr = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
                      req_to_token=cache.req_to_token, req_pool_indices=cache.req_pool_indices,
                      out_cache_loc=torch.tensor([3, -1], dtype=torch.int32, device="cuda"))
-    k2 = torch.zeros(2, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k2 = torch.zeros(2, hk, 128, dtype=torch.bfloat16, device="cuda")
     pkv.kv_write(wr, 1, k2, k2)
     assert pkv.last_device_error() == (_lib.PKV_ERR_INDEX, -1)
     # the context is still healthy and the word was cleared
     o = pkv.paged_decode(cache, 1, q, workspace=ws)
     no_device_error()
     assert_close(f64(o), oracle_decode(case), "bf16", "after errors")
+
+
+def _short_lens(kind):
+    rng = np.random.Generator(np.random.PCG64(len(kind)))
+    if kind == "uniform_0_12":        # 300 entries, a few pieces per CTA, empty ones among them
+        return rng.integers(0, 13, 300)
+    if kind == "clustered_ones":      # 500 x 40 tokens, then 500 x 1: ~135 pieces per CTA there
+        return np.array([40] * 500 + [1] * 500)
+    return rng.integers(0, 4, 1100)   # more than 1024 entries
+
+
+@pytest.mark.parametrize("kind", ["uniform_0_12", "clustered_ones", "over_1024"])
+def test_balanced_decode_many_short_entries(kind):
+    """Balanced plan over many short entries.  A CTA with at most 64 pieces
+    (in a batch of at most 1024 entries) stages all its slots and streams
+    across piece boundaries; the CTAs over the 1-token run of
+    "clustered_ones" hold ~135 pieces and every CTA of "over_1024" sees more
+    than 1024 entries, so those take the piece-by-piece pass.  Empty entries
+    give 0."""
+    kv = _short_lens(kind)
+    n_entries = kv.size
+    rng = np.random.Generator(np.random.PCG64(n_entries))
+    case = W.make_case("short", mode="decode", dtype="bf16", n_layers=1, layer_id=0, size=32768,
+                       n_heads=16, n_kv_heads=8, head_dim=128, kv_lens=kv,
+                       q_lens=(kv > 0).astype(np.int64), seed=n_entries)
+    case.q = W._values(rng, (n_entries, 16, 128), "bf16")
+    cache, qd = prepare(case)
+    ws = ws_for(case, splits=2)
+    assert pkv.decode_plan(cache, case.n_heads, ws)[0] == 0      # balanced
+    o = pkv.paged_decode(cache, case.layer_id, qd, workspace=ws)
+    no_device_error()
+    got = f64(o)
+    assert np.all(got[kv == 0] == 0.0), "empty context must give 0"
+    assert_close(got, oracle_decode(case), "bf16", kind)
+
+
+def test_balanced_decode_long_ranges():
+    """More than 2048 tokens per CTA (T > SMs * 2048): the slot indices of a
+    CTA no longer fit at once, so its pieces stream one by one."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_entries = 40
+    ctx = -(-sms * (2048 + 64) // n_entries)
+    case = W.make_case("longr", mode="decode", dtype="bf16", n_layers=1, layer_id=0,
+                       size=ctx * n_entries, n_heads=8, n_kv_heads=8, head_dim=64,
+                       kv_lens=[ctx] * n_entries, seed=9)
+    cache, q = prepare(case)
+    ws = ws_for(case, splits=8)
+    assert pkv.decode_plan(cache, case.n_heads, ws) == (0, sms)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "long ranges")
 
 
 def test_workspace_too_small_is_rejected():
