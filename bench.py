@@ -238,7 +238,8 @@ def prefill_flops(case) -> float:
 # ---------------------------------------------------------------------------
 
 class DecodeStep:
-    """Pre-marshalled C-ABI calls for one decode step (kv_write + paged_decode)."""
+    """Pre-marshalled C-ABI calls for one decode step: the fused pkv_decode_step,
+    or its two halves (pkv_kv_write, then pkv_paged_decode) for per-kernel times."""
 
     def __init__(self, lib, cache, q, kn, vn, o, ws, layer_id, chunk, stream):
         from paged_kv_cache_loc_gb300 import _lib
@@ -255,6 +256,11 @@ class DecodeStep:
         self.ws = ctypes.byref(ws.desc)
         self.s = ctypes.c_void_p(stream.cuda_stream)
         self.check = _lib.check
+
+    def fused(self):
+        self.check(self.lib.pkv_decode_step(self.cref, self.layer, self.k, self.v, self.n_new,
+                                            self.q, self.o, self.heads, self.scale, self.ws,
+                                            self.s), "pkv_decode_step")
 
     def write(self):
         self.check(self.lib.pkv_kv_write(self.cref, self.layer, self.k, self.v, self.n_new, self.s),
@@ -345,10 +351,20 @@ def run_pkv(args):
         sampler.start()
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        step_ms, parts = timed(torch, stream, None, args.steps, args.warmup, flush,
+        # the step as a user makes it: one pkv_decode_step call (the automatic
+        # plan), or the two calls when a split size is forced
+        if chunk == 0:
+            step_ms, _ = timed(torch, stream, step.fused, args.steps, args.warmup, flush)
+        else:
+            step_ms, _ = timed(torch, stream, None, args.steps, args.warmup, flush,
                                parts=[step.write, step.decode])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall0
+        # per-kernel times: the write and the decode as separate calls, each
+        # bracketed by events (these give the roofline of the decode kernels)
+        _, parts = timed(torch, stream, None, args.steps, args.warmup, flush,
+                         parts=[step.write, step.decode])
+        torch.cuda.synchronize()
         clocks = sampler.stop()
     st, detail = pkv.last_device_error(stream, dev)
     if st != 0:
@@ -403,6 +419,9 @@ def run_pkv(args):
         "kv_write_ms": round(ms_write, 5),
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
+        "step_call": ("pkv_decode_step (kv_write, then the decode split kernel as its programmatic "
+                      "dependent, then the merge)" if chunk == 0 else "pkv_kv_write + pkv_paged_decode_chunked"),
+        "decode_only_ms": round(ms_decode, 5),
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -422,8 +441,8 @@ def run_pkv(args):
 
 def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of q, k_new, v_new and the per-step metadata, kv_write +
-    paged_decode, D2H of o, all inside the events."""
+    memory: H2D of q, k_new, v_new and the per-step metadata, decode_step
+    (kv_write + paged_decode), D2H of o, all inside the events."""
     from paged_kv_cache_loc_gb300 import workloads as W
     hq = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
     hk = torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -442,8 +461,11 @@ def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     def step():
         for h, d in zip([hq, hk, hv] + meta, [dq, dk, dv] + dmeta):
             d.copy_(h, non_blocking=True)
-        pkv.kv_write(c, case.layer_id, dk, dv, stream=stream)
-        pkv.paged_decode(c, case.layer_id, dq, do, workspace=ws, chunk=chunk, stream=stream)
+        if chunk == 0:
+            pkv.decode_step(c, case.layer_id, dk, dv, dq, do, workspace=ws, stream=stream)
+        else:
+            pkv.kv_write(c, case.layer_id, dk, dv, stream=stream)
+            pkv.paged_decode(c, case.layer_id, dq, do, workspace=ws, chunk=chunk, stream=stream)
         ho.copy_(do, non_blocking=True)
 
     n = max(20, args.steps // 4)

@@ -189,6 +189,22 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
                      int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
 
 /*
+ * One decode step of a layer ("Attention Backend": the new tokens' K/V go
+ * into the cache, then attention reads it): pkv_kv_write of k_new / v_new
+ * (n_new rows at c->out_cache_loc, n_new may be 0) followed by
+ * pkv_paged_decode with the automatic plan.  Arguments, layouts, results and
+ * errors are those of the two calls made back to back on `stream`; both are
+ * validated before either is enqueued.  The tensor-core decode kernel is
+ * launched as a programmatic dependent of the write: it reads kv_indptr,
+ * req_pool_indices, seq_lens, req_to_token and q while the write runs and
+ * waits for the write before reading K/V rows.  Those inputs therefore follow
+ * plain stream order (the write never modifies them).
+ */
+int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, const void *v_new,
+                    int32_t n_new, const void *q, void *o, int32_t n_heads, float sm_scale,
+                    const pkv_workspace *ws, void *stream);
+
+/*
  * pkv_paged_decode with an explicit split size: every entry's context is cut
  * into chunks of `chunk` tokens (a positive multiple of 32; 0 = automatic).
  * The result is the same up to fp32 rounding for any chunk; the workspace

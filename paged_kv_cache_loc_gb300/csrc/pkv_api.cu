@@ -156,8 +156,12 @@ int make_plan(const pkv_kvcache *c, int32_t n_heads, int sms, const pkv_workspac
     return PKV_OK;
 }
 
-int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, int32_t n_heads,
-                float sm_scale, int32_t chunk, const pkv_workspace *ws, void *stream) {
+// Validates a decode call and fills its kernel parameters; *empty is set when
+// there is nothing to launch (batch 0).  Enqueues nothing.
+int decode_prepare(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
+                   int32_t n_heads, float sm_scale, int32_t chunk, const pkv_workspace *ws,
+                   pkv::DecodeParams *out, bool *empty) {
+    *empty = false;
     int rc = check_pool(c, layer_id);
     if (rc) return rc;
     rc = check_attn(c, n_heads, q, o);
@@ -166,7 +170,10 @@ int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, 
     if (!isfinite(sm_scale)) return PKV_ERR_ARG;
     const int group = n_heads / c->n_kv_heads;
     if (!pkv::decode_supported(c->dtype, c->head_dim, group)) return PKV_ERR_UNSUPPORTED;
-    if (c->batch == 0) return PKV_OK;
+    if (c->batch == 0) {
+        *empty = true;
+        return PKV_OK;
+    }
     if (q == o) return PKV_ERR_ARG;
     DeviceInfo di;
     rc = device_info(&di);
@@ -175,7 +182,8 @@ int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, 
     rc = make_plan(c, n_heads, di.sms, ws, chunk, &plan);
     if (rc) return rc;
 
-    pkv::DecodeParams p{};
+    pkv::DecodeParams &p = *out;
+    p = pkv::DecodeParams{};
     p.balanced = plan.balanced;
     p.n_parts = plan.n_parts;
     p.kv_indptr = c->kv_indptr;
@@ -209,17 +217,32 @@ int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, 
     p.n_splits = plan.n_splits;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.err = di.err;
-    return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, group,
+    return PKV_OK;
+}
+
+int decode_impl(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o, int32_t n_heads,
+                float sm_scale, int32_t chunk, const pkv_workspace *ws, void *stream) {
+    pkv::DecodeParams p;
+    bool empty = false;
+    int rc = decode_prepare(c, layer_id, q, o, n_heads, sm_scale, chunk, ws, &p, &empty);
+    if (rc || empty) return rc;
+    return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, p.n_heads / p.n_kv_heads,
                                          static_cast<cudaStream_t>(stream)));
 }
 
-int kv_write_impl(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
-                  int32_t n_new, const float *freqs_cis, int32_t max_pos,
-                  const int32_t *positions, bool rope, void *stream) {
+// Validates a cache write and fills its kernel parameters; *empty is set
+// when there is nothing to launch (n_new 0).  Enqueues nothing.
+int kv_write_prepare(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                     int32_t n_new, const float *freqs_cis, int32_t max_pos,
+                     const int32_t *positions, bool rope, pkv::KvWriteParams *out, bool *empty) {
+    *empty = false;
     int rc = check_pool(c, layer_id);
     if (rc) return rc;
     if (n_new < 0) return PKV_ERR_ARG;
-    if (n_new == 0) return PKV_OK;
+    if (n_new == 0) {
+        *empty = true;
+        return PKV_OK;
+    }
     if (!k || !v || !c->out_cache_loc || !aligned16(k) || !aligned16(v)) return PKV_ERR_ARG;
     const int64_t row_chunks =
         static_cast<int64_t>(c->n_kv_heads) * c->head_dim * elem_bytes(c->dtype) / 16;
@@ -231,7 +254,8 @@ int kv_write_impl(const pkv_kvcache *c, int32_t layer_id, const void *k, const v
     DeviceInfo di;
     rc = device_info(&di);
     if (rc) return rc;
-    pkv::KvWriteParams p{};
+    pkv::KvWriteParams &p = *out;
+    p = pkv::KvWriteParams{};
     p.k = k;
     p.v = v;
     p.k_buffer = c->k_buffer;
@@ -247,6 +271,17 @@ int kv_write_impl(const pkv_kvcache *c, int32_t layer_id, const void *k, const v
     p.positions = positions;
     p.max_pos = max_pos;
     p.err = di.err;
+    return PKV_OK;
+}
+
+int kv_write_impl(const pkv_kvcache *c, int32_t layer_id, const void *k, const void *v,
+                  int32_t n_new, const float *freqs_cis, int32_t max_pos,
+                  const int32_t *positions, bool rope, void *stream) {
+    pkv::KvWriteParams p;
+    bool empty = false;
+    int rc = kv_write_prepare(c, layer_id, k, v, n_new, freqs_cis, max_pos, positions, rope, &p,
+                              &empty);
+    if (rc || empty) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return map_launch(rope ? pkv::launch_rope_kv_write(p, s) : pkv::launch_kv_write(p, s));
 }
@@ -297,6 +332,32 @@ int pkv_rope_kv_write(const pkv_kvcache *c, int32_t layer_id, const void *k, con
 int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
                      int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream) {
     return decode_impl(c, layer_id, q, o, n_heads, sm_scale, 0, ws, stream);
+}
+
+int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, const void *v_new,
+                    int32_t n_new, const void *q, void *o, int32_t n_heads, float sm_scale,
+                    const pkv_workspace *ws, void *stream) {
+    // both calls are validated before either is enqueued
+    pkv::KvWriteParams wp;
+    bool no_write = false;
+    int rc = kv_write_prepare(c, layer_id, k_new, v_new, n_new, nullptr, 0, nullptr, false, &wp,
+                              &no_write);
+    if (rc) return rc;
+    pkv::DecodeParams dp;
+    bool no_decode = false;
+    rc = decode_prepare(c, layer_id, q, o, n_heads, sm_scale, 0, ws, &dp, &no_decode);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!no_write) {
+        rc = map_launch(pkv::launch_kv_write(wp, s));
+        if (rc) return rc;
+    }
+    if (no_decode) return PKV_OK;
+    // the tensor-core split kernels read metadata and q before waiting on
+    // the write; the others are launched in plain stream order
+    dp.pdl = !no_write && pkv::decode_balanced_supported(c->dtype, c->head_dim,
+                                                         n_heads / c->n_kv_heads, c->n_kv_heads);
+    return map_launch(pkv::launch_decode(dp, c->dtype, c->head_dim, n_heads / c->n_kv_heads, s));
 }
 
 int pkv_paged_decode_chunked(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,

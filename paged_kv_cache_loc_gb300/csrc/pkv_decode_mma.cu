@@ -100,6 +100,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
     return false;
 }
+// Wait for the grid this one depends on programmatically (the cache write
+// of a decode step) to complete and its writes to become visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // One bulk (TMA) copy of `bytes` contiguous bytes global -> shared, counted
 // on the mbarrier `bar`.  Addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -558,6 +562,7 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
         slots[j] = sl;
     }
     __syncthreads();
+    if (p.pdl) griddep_wait();   // K/V rows may come from the cache write before this kernel
 
     const int64_t slot_stride = static_cast<int64_t>(8) * D;
     const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + p.layer_row0 * slot_stride;
@@ -878,6 +883,7 @@ decode_mma_allheads_kernel(const DecodeParams p) {
     };
 
     if (!p.balanced) {
+        if (p.pdl) griddep_wait();
         const int split = blockIdx.x, b = blockIdx.y;
         int r = __ldg(p.req_pool_indices + b);
         if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
@@ -931,6 +937,7 @@ decode_mma_allheads_kernel(const DecodeParams p) {
             return;
     }
 
+    if (p.pdl) griddep_wait();   // piece-by-piece pass: wait before anything streams
     int lo_b = 0, hi_b = p.batch - 1;   // first entry whose range ends after t0
     while (lo_b < hi_b) {
         const int mid = (lo_b + hi_b) >> 1;
@@ -970,9 +977,17 @@ cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
-    dim3 grid = p.balanced ? dim3(p.n_parts, 1) : dim3(p.n_splits, p.batch);
-    decode_mma_allheads_kernel<D, G, HK><<<grid, C::kNTAH, C::kSmem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = p.balanced ? dim3(p.n_parts, 1) : dim3(p.n_splits, p.batch);
+    cfg.blockDim = dim3(C::kNTAH);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_mma_allheads_kernel<D, G, HK>, p);
 }
 
 template <int D, int G>

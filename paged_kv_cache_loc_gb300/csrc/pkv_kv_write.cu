@@ -8,6 +8,8 @@
 // row, so both the reads of k/v and the scattered row writes are fully
 // coalesced 16-byte accesses.  Each thread issues all of its loads before its
 // stores to keep several requests in flight.
+#include <atomic>
+
 #include "pkv_common.cuh"
 #include "pkv_launch.h"
 
@@ -18,6 +20,10 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams p) {
+    // A decode split kernel launched as a programmatic dependent of this write
+    // may start now: it reads metadata while the write runs and waits for this
+    // grid before reading K/V rows.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
     const int32_t total = 2 * per_buf;
     const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
@@ -78,6 +84,7 @@ __device__ __forceinline__ uint4 rotate_chunk_f32(uint4 x, const float *cs) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) rope_kv_write_kernel(const KvWriteParams p) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     constexpr int kElemsPerChunk = BF16 ? 8 : 4;
     const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
     const int32_t total = 2 * per_buf;
@@ -129,6 +136,21 @@ inline unsigned grid_for(const KvWriteParams &p) {
 
 cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s) {
     if (p.n_new == 0) return cudaSuccess;
+    // The write uses no shared memory.  With the carve-out at its shared
+    // maximum, the decode kernel that follows in a step (about 208 KB of
+    // shared memory per SM) fits beside it, and the SMs need no
+    // reconfiguration between the two.
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        e = cudaFuncSetAttribute(kv_write_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
     kv_write_kernel<<<grid_for(p), kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }

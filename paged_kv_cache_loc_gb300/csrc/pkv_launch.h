@@ -58,6 +58,10 @@ struct DecodeParams {
     const int32_t *kv_indptr;
     int32_t balanced;
     int32_t n_parts;
+    // 1: the split kernel is launched as a programmatic dependent of the
+    // cache write before it; it reads metadata, slot indices and q at once
+    // and waits (griddepcontrol.wait) before its first K/V row read.
+    int32_t pdl;
 };
 
 // Ragged causal prefill.

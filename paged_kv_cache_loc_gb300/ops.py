@@ -148,6 +148,31 @@ def paged_decode(cache: KVCache, layer_id: int, q: torch.Tensor, o: Optional[tor
     return o
 
 
+def decode_step(cache: KVCache, layer_id: int, k_new: torch.Tensor, v_new: torch.Tensor,
+                q: torch.Tensor, o: Optional[torch.Tensor] = None,
+                sm_scale: Optional[float] = None, workspace: Optional[Workspace] = None,
+                stream=None) -> torch.Tensor:
+    """kv_write of k_new / v_new at cache.out_cache_loc, then paged_decode
+    (automatic plan), as one call whose decode overlaps the write's launch."""
+    c = cache.c_struct()
+    dev = cache.device
+    n_heads, head_dim = int(q.shape[1]), int(q.shape[2])
+    if o is None:
+        o = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(head_dim) if sm_scale is None else float(sm_scale)
+    n_new = int(k_new.shape[0])
+    if v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must have the same shape")
+    rc = _lib.load().pkv_decode_step(ctypes.byref(c), layer_id,
+                                     _need(k_new, "k_new", cache.k_buffer.dtype, dev),
+                                     _need(v_new, "v_new", cache.k_buffer.dtype, dev), n_new,
+                                     _need(q, "q", cache.k_buffer.dtype, dev),
+                                     _need(o, "o", cache.k_buffer.dtype, dev), n_heads, scale,
+                                     _ws(workspace), _stream(stream, dev))
+    check(rc, "pkv_decode_step")
+    return o
+
+
 def paged_decode_noalloc(cache: KVCache, layer_id: int, q: torch.Tensor, o: torch.Tensor,
                          sm_scale: Optional[float] = None, stream=None) -> torch.Tensor:
     """paged_decode with the split partials in the library's fixed device array

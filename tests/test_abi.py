@@ -147,6 +147,20 @@ def test_kv_write_rejects_bad_arguments(lib):
     assert lib.pkv_rope_kv_write(ctypes.byref(c), 2, K, V, 4, F, 64, None, None) == _lib.PKV_ERR_ARG
 
 
+def test_decode_step_rejects_bad_arguments(lib):
+    """The step validates its write and its decode before enqueueing either."""
+    c = fake_cache()
+    K, V = ctypes.c_void_p(0xB00000), ctypes.c_void_p(0xC00000)
+    step = lib.pkv_decode_step
+    assert step(None, 2, K, V, 4, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert step(ctypes.byref(c), 2, K, V, -1, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert step(ctypes.byref(c), 9, K, V, 4, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert step(ctypes.byref(c), 2, None, V, 4, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    # nothing to write and an empty batch: nothing to do, no CUDA call
+    assert step(ctypes.byref(fake_cache(batch=0)), 2, K, V, 0, Q, O, 32, 0.1, None,
+                None) == _lib.PKV_OK
+
+
 def test_prefill_rejects_bad_arguments(lib):
     c = fake_cache(max_len=256)
 

@@ -443,6 +443,63 @@ def test_balanced_decode_replays_in_a_cuda_graph():
     assert_close(f64(o), ref, "bf16", "balanced graph replay")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_step_equals_write_then_decode(dtype):
+    """pkv_decode_step (the write, then the decode launched as its
+    programmatic dependent) leaves the pool the oracle's write gives and
+    returns o equal to kv_write followed by paged_decode.  Every context ends
+    with the token just written, so a decode that read K/V rows before the
+    write finished would miss it."""
+    if dtype == "bf16":
+        case = W.batched_decode(batch=16, lo=200, hi=3000, size=65536, seed=717)
+    else:
+        case = W.tiny_decode()
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    o = pkv.decode_step(cache, case.layer_id, kn, vn, q, workspace=ws)
+    no_device_error()
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    check_pool_bit_exact(cache, case)
+    assert_close(f64(o), oracle_decode(case), dtype, "decode step")
+    o2 = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    assert torch.equal(o, o2)
+
+
+def test_decode_step_replays_in_a_cuda_graph():
+    """The step captured once (its programmatic edge becomes a graph edge),
+    replayed after new K/V rows are put in the step's input buffers: the
+    decode sees the rows written in the same replay."""
+    case = W.batched_decode(batch=12, lo=50, hi=2500, size=32768, seed=818)
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    o = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.decode_step(cache, case.layer_id, kn, vn, q, o, workspace=ws, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    assert_close(f64(o), oracle_decode(case), "bf16", "step graph replay")
+    rng = np.random.Generator(np.random.PCG64(19))
+    for name in ("k_new", "v_new"):
+        bits = W._values(rng, getattr(case, name).shape, "bf16")
+        setattr(case, name, bits)
+        (kn if name == "k_new" else vn).copy_(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    check_pool_bit_exact(cache, case)
+    assert_close(f64(o), oracle_decode(case), "bf16", "step graph replay, new rows")
+
+
 def test_decode_on_slot_maps_from_the_page_pool():
     """req_to_token rows produced by the host allocator after churn (shared
     prefixes reused from the prefix cache, freed and evicted pages, decode
