@@ -7,25 +7,34 @@
 // qo_indptr[b] + i, head h attends to slots req_to_token[req_pool_indices[b], j]
 // for j <= P + i (P = kv_len - q_len) or j < kv_len when not causal.
 //
-// One CTA of 8 warps per (query tile, kv head, entry).  A query tile is 128
-// rows of (position, head-in-group) pairs, so the G query heads of a kv head
-// share every gathered K/V tile; warps w and w+4 share TMEM lanes 32(w%4)..
-// and split each row's columns in halves.  TMEM holds two S buffers and O, so
-// the tensor core computes S_{j+1} (and then P.V_j) while the threads run the
-// softmax of tile j.  Per 128-token K/V tile j:
-//   1. wait S_j (tcgen05.commit -> mbarrier), issue S_{j+1} = Q K_{j+1}^T
-//      (8 tcgen05.mma, M=128, N=128, K=16) into the other S buffer, and start
-//      gathering K_{j+2} (cp.async, slot indices staged in shared memory from
-//      a register prefetched ahead) into the K slot S_j just released;
-//   2. softmax: thread r reads its row of S_j with tcgen05.ld, keeps a running
-//      maximum that is only raised when the tile maximum exceeds it by more
-//      than 2^8 (then O and l are rescaled in TMEM, after P.V_{j-1} is done),
-//      and writes P = 2^(s - m) as bf16 into a 128-byte-swizzled K-major tile;
-//      V_{j+1} is gathered into the V slot P.V_{j-1} released;
-//   3. O += P V_j: 8 tcgen05.mma (V read MN-major) into TMEM.
-// Operand tiles use the 128-byte swizzle: a [rows x 128] bf16 tile is two
-// 64-column halves of rows x 128 B, 16-byte chunk c of row r stored at chunk
-// c ^ (r % 8), atoms 1024-byte aligned.  Every mbarrier wait is bounded.
+// One CTA of 16 warps per (pair of query tiles, kv head, entry).  A query
+// tile is 128 rows of (position, head-in-group) pairs; the CTA's two tiles A
+// and B (rows [256 i, 256 i + 128) and the next 128) share every gathered
+// K/V tile, which halves the gather traffic per flop -- a gather of random
+// 256-byte rows moves only ~30 GB/s per SM even from L2, so it is what bounds
+// this kernel.  The warps specialise and hand work over through mbarriers
+// (every wait bounded):
+//  - producer warps 8..14 (224 threads): each 128-token K and V tile is
+//    loaded with 16-byte loads (16 threads per 256-byte token row, slot
+//    indices staged in shared memory) into registers, then stored into a
+//    2-slot ring once the tensor core has released the slot;
+//  - MMA warp 15 (one thread) issues, per tile j,
+//      PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)     (S = Q K^T, O += P V),
+//    each of 8 tcgen05.mma (M=128, N=128, K=16), so the tensor core works on
+//    one query tile while the softmax runs on the other;
+//  - softmax warps 0..7: warps w and w+4 share TMEM lanes 32(w%4).. and take
+//    one 64-column half of each row.  A thread reads its scores of S_X(j) in
+//    two 32-column passes (the row maximum, exchanged with the other half
+//    through shared memory and a named barrier; then P), keeps a running
+//    maximum that is only raised when the tile maximum exceeds it by more
+//    than 2^8 (then its half of O_X is rescaled in TMEM -- P.V_X(j-1) is
+//    complete, as it was issued before S_X(j)), and stores P = 2^(s - m) as
+//    bf16 pairs over the S columns it has read; P.V reads P from TMEM as its
+//    A operand.
+// TMEM (512 columns): tile X in {A, B} has S (and P) at 256 X and O at
+// 256 X + 128.  Q, K and V tiles use the 128-byte swizzle: a [rows x 128]
+// bf16 tile is two 64-column halves of rows x 128 B, 16-byte chunk c of row
+// r stored at chunk c ^ (r % 8), atoms 1024-byte aligned.
 #include <atomic>
 
 #include "pkv_common.cuh"
@@ -34,21 +43,38 @@
 namespace pkv {
 namespace {
 
-constexpr int kRows = 128;       // query rows per CTA (TMEM lanes)
+constexpr int kRows = 128;       // query rows per query tile (TMEM lanes)
 constexpr int kTok = 128;        // kv tokens per tile
 constexpr int kD = 128;
-constexpr int kNT = 256;         // 8 warps: two threads per row, 64 columns each
-constexpr int kTileBytes = 128 * 128 * 2;                 // 32 KB: any [128 x 128] bf16 tile
-constexpr int kSmemQ = 0;
-constexpr int kSmemK = kTileBytes;                        // [2 slots] K tiles
-constexpr int kSmemV = kSmemK + 2 * kTileBytes;           // [2 slots] V tiles
-constexpr int kSmemP = kSmemV + 2 * kTileBytes;
-constexpr int kSmemBar = kSmemP + kTileBytes;             // mbarriers + tmem address
-constexpr int kSmemSlots = kSmemBar + 64;                 // [4][kTok] int slots of tiles
-constexpr int kSmemRed = kSmemSlots + 4 * 128 * 4;        // [2][kRows] float
-constexpr int kSmemBytes = kSmemRed + 2 * 128 * 4 + 1024; // + alignment slack
-constexpr uint32_t kTmemCols = 512;                       // S0: 0..127, S1: 128..255, O: 256..383
-constexpr float kRescale = 8.f;                           // lazy rescale threshold (log2 units)
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarps = 7;
+constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
+constexpr int kNT = (kMmaWarp + 1) * 32;                   // 512 threads
+constexpr int kPT = kProducerWarps * 32;                   // 224 producer threads
+constexpr int kChunks = (kTok * 16 + kPT - 1) / kPT;       // 16-byte chunks per producer thread and tile
+constexpr int kTileBytes = 128 * 128 * 2;                  // 32 KB: any [128 x 128] bf16 tile
+constexpr int kSmemQ = 0;                                  // [2] query tiles A, B
+constexpr int kSmemK = 2 * kTileBytes;                     // [2] K slots
+constexpr int kSmemV = kSmemK + 2 * kTileBytes;            // [2] V slots
+constexpr int kSmemBar = kSmemV + 2 * kTileBytes;
+// mbarriers
+constexpr int kBarKFull = 0;     // [2 slots] count kPT: producer threads
+constexpr int kBarKEmpty = 2;    // [2 slots] count 1: commit after the tile's S products
+constexpr int kBarVFull = 4;     // [2 slots] count kPT
+constexpr int kBarVEmpty = 6;    // [2 slots] count 1: commit after the tile's P.V products
+constexpr int kBarSFull = 8;     // [2 query tiles] count 1: S_X(j) complete
+constexpr int kBarPFull = 10;    // [2 query tiles] count 8: softmax warps have stored P_X(j)
+constexpr int kBarODone = 12;    // [2 query tiles] count 1: the last P.V_X complete
+constexpr int kNumBars = 14;
+constexpr int kSmemTmemAddr = kSmemBar + kNumBars * 8;
+constexpr int kSmemAbort = kSmemTmemAddr + 4;
+constexpr int kSmemRed = kSmemBar + 256;                   // [2 tiles][2 buffers][2 halves][kRows] float
+constexpr int kSmemSlots = kSmemRed + 2 * 2 * 2 * kRows * 4;   // [2][kTok] int: producer's slot indices
+constexpr int kSmemBytes = kSmemSlots + 2 * kTok * 4 + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescale = 8.f;                            // lazy rescale threshold (log2 units)
+static_assert(kSmemAbort + 4 <= kSmemRed, "barrier area");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // byte offset of 16-byte chunk `ch` (0..15) of row r
 __device__ __forceinline__ uint32_t sw_chunk(int r, int ch) {
@@ -104,18 +130,17 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
-// 64 consecutive fp32 columns of this thread's TMEM lane; the wait is in the
-// same asm block, so the values exist only once the load has completed
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-    uint32_t r[64];
+// 32 consecutive fp32 columns of this thread's TMEM lane (load and wait)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
@@ -134,23 +159,44 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
 }
 
+// O (f32, TMEM) += A (bf16 pairs in TMEM, lane = row) x B (shared-memory descriptor)
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+}
+
 template <int G>
 __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams p) {
     using bf16 = __nv_bfloat16;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t s_base = smem_u32(sm);
-    // bars[0], bars[1]: S buffer 0 / 1 complete; bars[2]: O (P.V) complete
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSmemBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kSmemBar + 32);
-    int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);          // [4][kTok]: tile t at t % 4
-    float *s_red = reinterpret_cast<float *>(sm + kSmemRed);         // [2 halves][kRows]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kSmemTmemAddr);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + kSmemAbort);
+    float *s_red = reinterpret_cast<float *>(sm + kSmemRed);
+    auto bar = [&](int i) -> uint32_t { return s_base + kSmemBar + 8 * i; };
 
     const int b = blockIdx.z, g = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;   // longest causal work first
+    const int qp = gridDim.x - 1 - blockIdx.x;   // longest causal work first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row = (warp & 3) * 32 + lane;     // TMEM lane = query row of this thread
-    const int hc = warp >> 2;                    // column half this thread handles
 
     int r = __ldg(p.req_pool_indices + b);
     const int qo0 = __ldg(p.qo_indptr + b);
@@ -158,74 +204,43 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
     if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 ||
         q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
-        if (qt == 0 && g == 0 && tid == 0)
+        if (qp == 0 && g == 0 && tid == 0)
             record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r : kv_len);
         return;
     }
     const int rows = q_len * G;
-    const int row0 = qt * kRows;
+    const int row0 = qp * 2 * kRows;
     if (row0 >= rows) return;
     const int P = kv_len - q_len;
-    const int pos_last = (min(row0 + kRows, rows) - 1) / G;
-    const int kv_end = p.causal ? min(kv_len, P + pos_last + 1) : kv_len;
-    const int n_tiles = (kv_end + kTok - 1) / kTok;
+    // K/V tiles each query tile sees (0: the tile has no rows); B sees at least as many as A
+    int n_x[2], kv_end = 0;
+#pragma unroll
+    for (int X = 0; X < 2; ++X) {
+        const int rx = row0 + X * kRows;
+        n_x[X] = 0;
+        if (rx < rows) {
+            const int pos_last = (min(rx + kRows, rows) - 1) / G;
+            const int e = p.causal ? min(kv_len, P + pos_last + 1) : kv_len;
+            n_x[X] = (e + kTok - 1) / kTok;
+            kv_end = max(kv_end, e);
+        }
+    }
+    const int n_tiles = max(n_x[0], n_x[1]);   // >= 1: kv_end >= 1 when rows > 0
 
     const int64_t slot_stride = static_cast<int64_t>(p.n_kv_heads) * kD;
     const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
     const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
     const int32_t *r2t = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len;
 
-    // slot of token tid of tile `tile` (threads 0..kTok-1), 0 past the visible range
-    auto fetch_slot = [&](int tile) -> int {
-        const int j = tile * kTok + tid;
-        if (tid >= kTok || tile >= n_tiles || j >= kv_end) return 0;
-        int slot = __ldg(r2t + j);
-        if (static_cast<unsigned long long>(static_cast<long long>(slot)) >=
-            static_cast<unsigned long long>(p.size)) {
-            record_error(p.err, slot);
-            slot = 0;
-        }
-        return slot;
-    };
-    // gather K (is_v = 0) or V rows of tile `tile` into ring slot tile % 2
-    auto load_tile = [&](int tile, int is_v) {
-        const int j0 = tile * kTok;
-        const int *slots = s_slot + (tile & 3) * kTok;
-        unsigned char *dst0 = sm + (is_v ? kSmemV : kSmemK) + (tile & 1) * kTileBytes;
-        const bf16 *base = is_v ? vbase : kbase;
-#pragma unroll 8
-        for (int i = tid; i < kTok * 16; i += kNT) {
-            const int t = i >> 4, ch = i & 15;
-            void *dst = dst0 + sw_chunk(t, ch);
-            if (j0 + t < kv_end)
-                cp_async16(dst, base + slots[t] * slot_stride + ch * 8);
-            else
-                cp_async16(dst, kbase, 0);
-        }
-    };
-    auto issue_s = [&](int tile) {   // thread 0: S[tile % 2] = Q K_tile^T
-        fence_after();
-        const uint32_t kaddr = s_base + kSmemK + (tile & 1) * kTileBytes;
-        const uint32_t id_s = idesc(128, 128, 0);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-            mma_f16(*tmem_slot + (tile & 1) * 128, sdesc(s_base + kSmemQ + off, 16, 1024),
-                    sdesc(kaddr + off, 16, 1024), id_s, ks > 0);
-        }
-        mma_commit(smem_u32(bars + (tile & 1)));
-    };
-
-    // ---- prologue: slots of tiles 0..2, Q + K0, K1, V0
-    if (tid < kTok) {
-        s_slot[tid] = fetch_slot(0);
-        s_slot[kTok + tid] = fetch_slot(1);
-        s_slot[2 * kTok + tid] = fetch_slot(2);
-    }
-    int slot_next = fetch_slot(3);
+    // ---- setup: barriers, TMEM, the two query tiles
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bars + i)));
+        for (int i = 0; i < kNumBars; ++i) {
+            uint32_t cnt = 1;
+            if (i == kBarKFull || i == kBarKFull + 1 || i == kBarVFull || i == kBarVFull + 1) cnt = kPT;
+            else if (i == kBarPFull || i == kBarPFull + 1) cnt = kSoftmaxWarps;
+            mbar_init(bar(i), cnt);
+        }
+        *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 0) {
@@ -236,10 +251,10 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     }
     {
         const bf16 *q = static_cast<const bf16 *>(p.q);
-        for (int i = tid; i < kRows * 16; i += kNT) {
-            const int rr = i >> 4, ch = i & 15;
-            const int Rq = row0 + rr;
-            void *dst = sm + kSmemQ + sw_chunk(rr, ch);
+        for (int i = tid; i < 2 * kRows * 16; i += kNT) {
+            const int X = i / (kRows * 16), rr = (i >> 4) & (kRows - 1), ch = i & 15;
+            const int Rq = row0 + X * kRows + rr;
+            void *dst = sm + kSmemQ + X * kTileBytes + sw_chunk(rr, ch);
             if (Rq < rows) {
                 const int pos = Rq / G, hh = Rq - (Rq / G) * G;
                 cp_async16(dst, q + ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + ch * 8);
@@ -247,174 +262,275 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 cp_async16(dst, q, 0);
             }
         }
+        cp_async_commit();
+        cp_async_wait<0>();
     }
-    fence_before();
-    __syncthreads();   // slots of tiles 0..2 and the TMEM address are visible
-    fence_after();
-    load_tile(0, 0);
-    cp_async_commit();            // group: Q + K0
-    if (n_tiles > 1) load_tile(1, 0);
-    cp_async_commit();            // group: K1
-    load_tile(0, 1);
-    cp_async_commit();            // group: V0
-    cp_async_wait<0>();
     fence_async_smem();
-    __syncthreads();
-    if (tid == 0) issue_s(0);
-
+    fence_before();
+    __syncthreads();   // barriers, the TMEM address and the query tiles are visible
+    fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;   // this warp's TMEM lanes
-    const uint32_t tO = tmem + 256 + lane_off + hc * 64;
-    const int R = row0 + row;
-    const int lim = R < rows ? (p.causal ? P + R / G : kv_len - 1) : -1;   // last visible position
-    float m_run = -INFINITY, l_part = 0.f;   // l_part: this thread's 64 columns only
-    bool ok = true;
-    const uint32_t id_o = idesc(128, 128, 1);
 
-    // Iteration j: S_j is in flight (or done); the tensor core queue is
-    // [.. S_j, P.V_{j-1}]; we add S_{j+1} before the softmax of tile j.
-    for (int j = 0; j < n_tiles && ok; ++j) {
-        const uint32_t tS = tmem + (j & 1) * 128 + lane_off + hc * 64;
-        // K_{j+1} (group issued one iteration ago) must have landed for S_{j+1}
-        if (j >= 1) cp_async_wait<1>();
-        fence_async_smem();
-        // S_j complete: the threads may read it; its K slot is free.
-        ok = __syncthreads_and(bar_wait(smem_u32(bars + (j & 1)), (j >> 1) & 1)) != 0;
-        fence_after();
-        if (!ok) break;
-        if (tid == 0 && j + 1 < n_tiles) issue_s(j + 1);
-        // next tiles' slots and the K_{j+2} gather (into the slot S_j just freed)
-        if (tid < kTok) s_slot[((j + 3) & 3) * kTok + tid] = slot_next;
-        slot_next = fetch_slot(j + 4);
-        if (j + 2 < n_tiles) load_tile(j + 2, 0);
-        cp_async_commit();        // group A_j: K_{j+2}
-
-        // ---- softmax: this thread's row, columns [64 hc, 64 hc + 64)
-        const int jt = j * kTok + hc * 64;
-        const bool need_mask = jt + 63 > lim;
-        float sv[64];   // this thread's 64 scores, read once
-        tmem_ld64(tS, sv);
-        if (need_mask) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                if (jt + i > lim) sv[i] = -INFINITY;
-        }
-        float mx[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        float mt = mraw * p.scale_log2;   // -inf stays -inf
-        s_red[hc * kRows + row] = mt;
-        // P.V_{j-1} must be complete before O is rescaled and P is rewritten;
-        // then its V slot takes V_{j+1}.
-        const bool o_ok = j == 0 || bar_wait(smem_u32(bars + 2), (j - 1) & 1);
-        ok = __syncthreads_and(o_ok) != 0;
-        fence_after();
-        if (!ok) break;
-        if (j + 1 < n_tiles) load_tile(j + 1, 1);
-        cp_async_commit();        // group B_j: V_{j+1}
-        mt = fmaxf(mt, s_red[(hc ^ 1) * kRows + row]);
-        // Raise the reference only when the tile maximum exceeds it by more than
-        // 2^8, so that P stays <= 2^8 and O is rescaled rarely.  TMEM accesses
-        // are warp-collective: a warp rescales if any of its rows must.
-        const bool raise = mt > m_run + kRescale || (m_run == -INFINITY && mt != -INFINITY);
-        const float alpha = raise ? exp2f(m_run - mt) : 1.f;   // 0 on the first visible tile
-        const bool touch_o = raise && j > 0 && m_run != -INFINITY;
-        if (__any_sync(0xffffffffu, touch_o)) {
-            const float f = touch_o ? alpha : 1.f;
-            float ov[64];
-            tmem_ld64(tO, ov);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = ov[h2 * 32 + i] * f;
-                tmem_st32(tO + h2 * 32, v);
+    if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
+        // ================= producer: K and V tile t into ring slot t % 2
+        const int pt = tid - kSoftmaxWarps * 32;
+        int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
+        auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
+            const int j = tile * kTok + pt;
+            if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
+            int slot = __ldg(r2t + j);
+            if (static_cast<unsigned long long>(static_cast<long long>(slot)) >=
+                static_cast<unsigned long long>(p.size)) {
+                record_error(p.err, slot);
+                slot = 0;
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        }
-        if (raise) {
-            l_part *= alpha;
-            m_run = mt;
-        }
-        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // a row with nothing visible yet keeps P = 0: its reference is -inf and
-        // fma(v, scale, -inf) = -inf for finite or -inf v
-        const float neg_m = m_run == -INFINITY ? -INFINITY : -m_run;
-        const float sc = p.scale_log2;
+            return slot;
+        };
+        int slot_n = fetch(0);
+        // A wait that gives up sets the abort flag; after that nothing is
+        // stored, but every producer barrier is still met.
+        for (int t = 0; t < n_tiles; ++t) {
+            int *slots = s_slot + (t & 1) * kTok;
+            if (pt < kTok) slots[pt] = slot_n;
+            slot_n = fetch(t + 1);   // the next tile's index is in flight meanwhile
+            named_sync(1, kPT);      // this tile's slots are staged
+            uint4 kv[2][kChunks];
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = ex2_approx(fmaf(sv[c0 + i], sc, neg_m));
-                const float p1 = ex2_approx(fmaf(sv[c0 + i + 1], sc, neg_m));
-                ls[(i >> 1) & 7] += p0 + p1;
-                __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+            for (int k = 0; k < kChunks; ++k) {
+                const int i = pt + k * kPT;
+                kv[0][k] = kv[1][k] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < kTok * 16) {
+                    const int sl = slots[i >> 4];
+                    if (sl >= 0) {
+                        const int64_t off = sl * slot_stride + (i & 15) * 8;
+                        kv[0][k] = __ldcg(reinterpret_cast<const uint4 *>(kbase + off));
+                        kv[1][k] = __ldcg(reinterpret_cast<const uint4 *>(vbase + off));
+                    }
+                }
             }
+            bool live = *s_abort == 0 && bar_wait(bar(kBarKEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4 *>(sm + kSmemP + sw_chunk(row, hc * 8 + (c0 >> 3) + q4)) =
-                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
-        l_part += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        // V_j (group B_{j-1}) must have landed: newer groups are A_j and B_j
-        cp_async_wait<2>();
-        fence_async_smem();   // P and V_j (generic writes) -> visible to the tensor core
-        fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after();
-            const uint32_t vaddr = s_base + kSmemV + (j & 1) * kTileBytes;
+            for (int X = 0; X < 2; ++X) {   // X = 0: K, 1: V
+                if (X == 1) live = live && bar_wait(bar(kBarVEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
+                if (!live) break;
+                unsigned char *dst0 = sm + (X ? kSmemV : kSmemK) + (t & 1) * kTileBytes;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t poff = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-                mma_f16(tmem + 256, sdesc(s_base + kSmemP + poff, 16, 1024),
-                        sdesc(vaddr + ks * 16 * 128, 128 * 128, 1024), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+                for (int k = 0; k < kChunks; ++k) {
+                    const int i = pt + k * kPT;
+                    if (i < kTok * 16) *reinterpret_cast<uint4 *>(dst0 + sw_chunk(i >> 4, i & 15)) = kv[X][k];
+                }
+                fence_async_smem();   // these generic stores -> the tensor core's reads
+                mbar_arrive(bar((X ? kBarVFull : kBarKFull) + (t & 1)));
             }
-            mma_commit(smem_u32(bars + 2));
+            if (!live && *s_abort == 0) {
+                *s_abort = 1;
+                record_error(p.err, -3001);
+            }
         }
-    }
-    // last P.V
-    if (ok && n_tiles > 0) {
-        ok = __syncthreads_and(bar_wait(smem_u32(bars + 2), (n_tiles - 1) & 1)) != 0;
-        fence_after();
-    }
-    if (!ok) {
-        if (tid == 0) record_error(p.err, -3000);
+    } else if (warp == kMmaWarp) {
+        // ================= MMA issue
+        if (lane == 0) {
+            const uint32_t id_s = idesc(128, 128, 0), id_o = idesc(128, 128, 1);
+            auto issue_s = [&](int X, int slot) {   // S_X = Q_X K^T
+                const uint32_t qaddr = s_base + kSmemQ + X * kTileBytes;
+                const uint32_t kaddr = s_base + kSmemK + slot * kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
+                    mma_f16(tmem + X * 256, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + off, 16, 1024), id_s,
+                            ks > 0);
+                }
+                mma_commit(bar(kBarSFull + X));
+            };
+            auto issue_pv = [&](int X, int slot, bool acc) {   // O_X += P_X V; P over S_X's columns
+                const uint32_t vaddr = s_base + kSmemV + slot * kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    // tokens [16 ks, 16 ks + 16): half ks / 4 of the row, packed at its first 32 columns
+                    const uint32_t pcol = (ks >> 2) * 64 + (ks & 3) * 8;
+                    mma_f16_ta(tmem + X * 256 + 128, tmem + X * 256 + pcol,
+                               sdesc(vaddr + ks * 16 * 128, 128 * 128, 1024), id_o, (acc || ks > 0) ? 1u : 0u);
+                }
+            };
+            auto give_up = [&](int code) {
+                *s_abort = 1;
+                record_error(p.err, code);
+            };
+            bool ok = bar_wait(bar(kBarKFull), 0);
+            if (!ok) give_up(-3002);
+            if (ok) {
+                fence_after();
+                issue_s(0, 0);
+                if (n_x[1] > 0) issue_s(1, 0);
+                mma_commit(bar(kBarKEmpty));
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (*s_abort) break;
+                const bool more = j + 1 < n_tiles;
+                if (!bar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1)) { give_up(-3003); break; }
+                if (j < n_x[0]) {
+                    if (!bar_wait(bar(kBarPFull), j & 1)) { give_up(-3004); break; }
+                    fence_after();
+                    issue_pv(0, j & 1, j > 0);
+                    if (j == n_x[0] - 1) mma_commit(bar(kBarODone));
+                }
+                if (more) {
+                    if (!bar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) { give_up(-3005); break; }
+                    fence_after();
+                    if (j + 1 < n_x[0]) issue_s(0, (j + 1) & 1);
+                }
+                if (j < n_x[1]) {
+                    if (!bar_wait(bar(kBarPFull + 1), j & 1)) { give_up(-3006); break; }
+                    fence_after();
+                    issue_pv(1, j & 1, j > 0);
+                    if (j == n_x[1] - 1) mma_commit(bar(kBarODone + 1));
+                }
+                mma_commit(bar(kBarVEmpty + (j & 1)));
+                if (more) {
+                    if (j + 1 < n_x[1]) issue_s(1, (j + 1) & 1);
+                    mma_commit(bar(kBarKEmpty + ((j + 1) & 1)));
+                }
+            }
+        }
+        __syncwarp();
     } else {
-        s_red[hc * kRows + row] = l_part;
-        __syncthreads();
-        const float l_row = l_part + s_red[(hc ^ 1) * kRows + row];
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        // every thread reads its lane (tcgen05.ld is warp-collective); rows past
-        // the request are not stored
-        const int pos = R / G, hh = R - (R / G) * G;
-        bf16 *orow = static_cast<bf16 *>(p.o) +
-                     ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + hc * 64;
-        float ov[64];
-        tmem_ld64(tO, ov);
+        // ================= softmax: row `row`, columns [64 hc, 64 hc + 64) of each tile
+        const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row of this thread
+        const int hc = warp >> 2;                  // column half
+        const int pair_bar = 2 + (warp & 3);       // named barrier of warps w and w + 4
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float sc = p.scale_log2;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};   // l: this half's columns
+        int lim[2];
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(ov[c0 + i] * inv, ov[c0 + i + 1] * inv);
-                pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+        for (int X = 0; X < 2; ++X) {
+            const int R = row0 + X * kRows + row;
+            lim[X] = R < rows ? (p.causal ? P + R / G : kv_len - 1) : -1;   // last visible position
+        }
+        // A wait that gives up sets the abort flag; after that no wait is made,
+        // but every named barrier is still met so the pair stays in step.
+        auto wait_ok = [&](uint32_t br, uint32_t par) -> bool {
+            bool ok = *s_abort == 0 && bar_wait(br, par);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0 && *s_abort == 0) {
+                *s_abort = 1;
+                record_error(p.err, -3007);
             }
-            if (R < rows) {
+            return ok;
+        };
+        for (int j = 0; j < n_tiles; ++j) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(orow + c0 + q4 * 8) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            for (int X = 0; X < 2; ++X) {
+                if (j >= n_x[X]) continue;   // CTA-uniform
+                wait_ok(bar(kBarSFull + X), j & 1);
+                fence_after();
+                const uint32_t tS = tmem + X * 256 + lane_off + hc * 64;
+                const int jt = j * kTok + hc * 64;
+                // pass 1: the row maximum of this half
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float v[32];
+                    tmem_ld32(tS + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx[i & 7] = fmaxf(mx[i & 7], jt + c * 32 + i > lim[X] ? -INFINITY : v[i]);
+                }
+                float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;   // -inf stays -inf
+                float *red = s_red + (X * 2 + (j & 1)) * 2 * kRows;
+                red[hc * kRows + row] = mt;
+                named_sync(pair_bar, 64);
+                mt = fmaxf(mt, red[(hc ^ 1) * kRows + row]);
+                // Raise the reference only when the tile maximum exceeds it by
+                // more than 2^8, so P stays <= 2^8 and O is rescaled rarely.  TMEM
+                // access is warp-collective: a warp rescales if any row must.
+                const bool raise = mt > m_run[X] + kRescale || (m_run[X] == -INFINITY && mt != -INFINITY);
+                const float alpha = raise ? exp2f(m_run[X] - mt) : 1.f;   // 0 on the first visible tile
+                const bool touch_o = raise && j > 0 && m_run[X] != -INFINITY;
+                if (__any_sync(0xffffffffu, touch_o)) {
+                    const float f = touch_o ? alpha : 1.f;
+                    const uint32_t tO = tmem + X * 256 + 128 + lane_off + hc * 64;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float v[32];
+                        tmem_ld32(tO + h2 * 32, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= f;
+                        tmem_st32(tO + h2 * 32, v);
+                    }
+                }
+                if (raise) {
+                    l_part[X] *= alpha;
+                    m_run[X] = mt;
+                }
+                // pass 2: P = 2^(s - m) as bf16 pairs over the columns just read;
+                // a row with nothing visible yet keeps P = 0 (reference -inf,
+                // fma(v, scale, -inf) = -inf for finite or -inf v)
+                const float neg_m = m_run[X] == -INFINITY ? -INFINITY : -m_run[X];
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float v[32];
+                    tmem_ld32(tS + c * 32, v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float s0 = jt + c * 32 + i > lim[X] ? -INFINITY : v[i];
+                        const float s1 = jt + c * 32 + i + 1 > lim[X] ? -INFINITY : v[i + 1];
+                        const float p0 = ex2_approx(fmaf(s0, sc, neg_m));
+                        const float p1 = ex2_approx(fmaf(s1, sc, neg_m));
+                        ls[(i >> 1) & 7] += p0 + p1;
+                        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                        pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    tmem_st16u(tS + c * 16, pk);
+                }
+                l_part[X] += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarPFull + X));   // P_X(j) and the rescaled O_X ready
+            }
+        }
+        // ---- epilogue: O_X is final once its last P.V is done
+#pragma unroll
+        for (int X = 0; X < 2; ++X) {
+            if (n_x[X] == 0) continue;
+            const bool done = wait_ok(bar(kBarODone + X), 0);
+            fence_after();
+            float *red = s_red + (X * 2 + (n_x[X] & 1)) * 2 * kRows;   // the buffer the last tile did not use
+            red[hc * kRows + row] = l_part[X];
+            named_sync(pair_bar, 64);
+            const float l_row = l_part[X] + red[(hc ^ 1) * kRows + row];
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            const int R = row0 + X * kRows + row;
+            const int pos = R / G, hh = R - (R / G) * G;
+            bf16 *orow = static_cast<bf16 *>(p.o) +
+                         ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + hc * 64;
+            // every thread reads its lane (tcgen05.ld is warp-collective); rows
+            // past the request are not stored
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float ov[32];
+                tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * 64 + c0, ov);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
+                    pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                if (done && *s_abort == 0 && R < rows) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<uint4 *>(orow + c0 + q4 * 8) =
+                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
             }
         }
     }
-    cp_async_wait<0>();
     fence_before();
     __syncthreads();
     if (warp == 0)
@@ -434,7 +550,7 @@ cudaError_t run(const PrefillParams &p, cudaStream_t s) {
         attr_done.fetch_or(bit);
     }
     const int qtiles = (p.max_q_len * G + kRows - 1) / kRows;
-    dim3 grid(qtiles, p.n_kv_heads, p.batch);
+    dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
     prefill_tc_kernel<G><<<grid, kNT, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
