@@ -429,6 +429,7 @@ def run_pkv(args):
     if not args.no_extras:
         out["e2e"] = e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev)
         out["long_context_b1"] = long_context_leg(torch, pkv, W, stream, flush, peaks, dev)
+        out["prefix_shared_pages"] = prefix_shared_leg(torch, pkv, W, stream, flush, peaks, dev)
         out["prefill"] = prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev)
     if rank == 0 and not args.no_extras:
         out["cpu_baseline"] = cpu_baseline(case, b_dec + b_wr)
@@ -508,6 +509,42 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
     out = dict(sweep[-1])
     out["sweep"] = [{k: s[k] for k in ("context", "us_per_decode", "kv_gbs", "frac_of_hbm_peak")}
                     for s in sweep]
+    return out
+
+
+def prefix_shared_leg(torch, pkv, W, stream, flush, peaks, dev):
+    """The prefix-shared workload (64 requests reading the same 2048-slot
+    prefix, private tails in 16-slot pages) decoded through the page table.
+    Logical bytes count every request's rows; unique bytes count each slot
+    once.  Timed with the L2 flushed before each call and without (then the
+    shared prefix stays in L2)."""
+    case = W.prefix_shared_decode()
+    cache, q, kn, vn = W.upload(case, dev)
+    pkv.kv_write(cache, case.layer_id, kn, vn)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024, device=dev)
+    o = torch.empty_like(q)
+    ps = case.page_size
+    table = torch.from_numpy(np.ascontiguousarray(case.req_to_token[:, ::ps] // ps)).to(dev)
+    used = np.unique(np.concatenate([case.slots_of(b) for b in range(case.batch)]))
+    row = case.n_kv_heads * case.head_dim * case.elem_bytes
+    logical = decode_bytes(case)
+    unique = float(used.size) * 2 * row + float(case.seq_lens.sum()) * 4 + \
+        2.0 * case.batch * case.n_heads * case.head_dim * case.elem_bytes
+    call = lambda: pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, o, workspace=ws,
+                                          stream=stream)
+    out = {"batch": case.batch, "page_size": ps, "shared_prefix_tokens": case.shared_prefix,
+           "logical_bytes": logical, "unique_bytes": unique}
+    with torch.cuda.stream(stream):
+        for name, fl in (("l2_flushed", flush), ("l2_warm", lambda: None)):
+            ms, _ = timed(torch, stream, call, 100, 10, fl)
+            t = statistics.median(ms)
+            out[name] = {"us_per_decode": round(t * 1e3, 2),
+                         "logical_gbs": round(logical / (t * 1e-3) / 1e9, 1),
+                         "unique_gbs": round(unique / (t * 1e-3) / 1e9, 1),
+                         "unique_frac_of_hbm_peak": round(unique / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    st, detail = pkv.last_device_error(stream, dev)
+    if st != 0:
+        raise RuntimeError(f"device error word set in the prefix-shared leg (detail {detail})")
     return out
 
 

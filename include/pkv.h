@@ -189,6 +189,26 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
                      int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
 
 /*
+ * Paged decode through a page table ("KVCache System": the pool is made of
+ * pages of page_size consecutive token slots; the 5-D view [n_layers,
+ * n_pages, page_size, n_kv_heads, head_dim] is byte-identical to
+ * c->k_buffer's [n_layers, size, n_kv_heads, head_dim] with size = n_pages *
+ * page_size).  Position j of entry b reads slot
+ *   req_to_page[r * max_pages + j / page_size] * page_size + j % page_size,
+ * r = c->req_pool_indices[b]; a 16-token stage of the kernel is then a run of
+ * consecutive slots.  req_to_page: int32 [c->num_reqs, max_pages] device
+ * array (c->num_reqs is its row count); c->req_to_token and c->max_ctx_len
+ * are not read.  Otherwise the operation, arguments, results and plan are
+ * those of pkv_paged_decode, with c->max_len <= max_pages * page_size.
+ * Requires c->size to be a multiple of page_size.  Supported: bf16,
+ * head_dim 64 or 128, G and n_kv_heads in {1, 2, 4, 8}.  A page index
+ * outside [0, size / page_size) is a device-data error.
+ */
+int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t *req_to_page,
+                           int32_t max_pages, int32_t page_size, const void *q, void *o,
+                           int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
+
+/*
  * One decode step of a layer ("Attention Backend": the new tokens' K/V go
  * into the cache, then attention reads it): pkv_kv_write of k_new / v_new
  * (n_new rows at c->out_cache_loc, n_new may be 0) followed by

@@ -334,6 +334,32 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
     return decode_impl(c, layer_id, q, o, n_heads, sm_scale, 0, ws, stream);
 }
 
+int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t *req_to_page,
+                           int32_t max_pages, int32_t page_size, const void *q, void *o,
+                           int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream) {
+    if (!c || !req_to_page || max_pages <= 0 || page_size <= 0) return PKV_ERR_ARG;
+    if (c->size <= 0 || c->size % page_size) return PKV_ERR_ARG;
+    if (static_cast<int64_t>(max_pages) * page_size > INT32_MAX) return PKV_ERR_ARG;
+    // the cache as the decode sees it: positions reach max_pages * page_size
+    // and request rows index the page table; req_to_token is not read
+    pkv_kvcache cc = *c;
+    cc.req_to_token = req_to_page;
+    cc.max_ctx_len = max_pages * page_size;
+    pkv::DecodeParams p;
+    bool empty = false;
+    int rc = decode_prepare(&cc, layer_id, q, o, n_heads, sm_scale, 0, ws, &p, &empty);
+    if (rc || empty) return rc;
+    if (!pkv::decode_balanced_supported(c->dtype, c->head_dim, n_heads / c->n_kv_heads, c->n_kv_heads))
+        return PKV_ERR_UNSUPPORTED;
+    p.req_to_token = nullptr;
+    p.req_to_page = req_to_page;
+    p.max_pages = max_pages;
+    p.page_size = page_size;
+    p.n_pages = c->size / page_size;
+    return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, n_heads / c->n_kv_heads,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, const void *v_new,
                     int32_t n_new, const void *q, void *o, int32_t n_heads, float sm_scale,
                     const pkv_workspace *ws, void *stream) {

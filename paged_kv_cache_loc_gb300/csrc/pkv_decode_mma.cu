@@ -423,6 +423,27 @@ __device__ __forceinline__ void block_math(const __nv_bfloat16 *kt, const __nv_b
     }
 }
 
+// Slot of position j of request row r: through req_to_token, or through the
+// page table when p.page_size > 0.  A slot or page outside the pool is
+// recorded and replaced by 0.
+__device__ __forceinline__ int slot_at(const DecodeParams &p, int r, int j) {
+    if (p.page_size > 0) {
+        const int pg = __ldg(p.req_to_page + static_cast<int64_t>(r) * p.max_pages + j / p.page_size);
+        if (static_cast<unsigned long long>(static_cast<long long>(pg)) >=
+            static_cast<unsigned long long>(p.n_pages)) {
+            record_error(p.err, pg);
+            return 0;
+        }
+        return pg * p.page_size + j % p.page_size;
+    }
+    int sl = __ldg(p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len + j);
+    if (static_cast<unsigned long long>(static_cast<long long>(sl)) >= static_cast<unsigned long long>(p.size)) {
+        record_error(p.err, sl);
+        sl = 0;
+    }
+    return sl;
+}
+
 // First CTA index of the balanced partition whose range holds token t.
 __device__ __forceinline__ int part_of(long long t, long long T, int P) {
     const long long c = ((t + 1) * P - 1) / T;
@@ -553,13 +574,7 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
             if (s_off[mid] <= j) a = mid; else z = mid - 1;
         }
         const int pos = min(j - s_off[a], s_len[a] - 1);
-        int sl = __ldg(p.req_to_token + static_cast<int64_t>(s_r[a]) * p.max_ctx_len + s_s0[a] + pos);
-        if (static_cast<unsigned long long>(static_cast<long long>(sl)) >=
-            static_cast<unsigned long long>(p.size)) {
-            record_error(p.err, sl);
-            sl = 0;
-        }
-        slots[j] = sl;
+        slots[j] = slot_at(p, s_r[a], s_s0[a] + pos);
     }
     __syncthreads();
     if (p.pdl) griddep_wait();   // K/V rows may come from the cache write before this kernel
@@ -736,19 +751,9 @@ decode_mma_allheads_kernel(const DecodeParams p) {
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        const int32_t *r2t = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len;
-
         for (int pc = s0; pc < s1; pc += kDecodeMaxChunk) {
             const int len = min(kDecodeMaxChunk, s1 - pc);
-            for (int j = tid; j < len; j += NT) {
-                int sl = __ldg(r2t + pc + j);
-                if (static_cast<unsigned long long>(static_cast<long long>(sl)) >=
-                    static_cast<unsigned long long>(p.size)) {
-                    record_error(p.err, sl);
-                    sl = 0;
-                }
-                slots[j] = sl;
-            }
+            for (int j = tid; j < len; j += NT) slots[j] = slot_at(p, r, pc + j);
             __syncthreads();
             const int nst = (len + C::kTS - 1) / C::kTS;
             const uint32_t first = issued;   // global index of this piece's stage 0

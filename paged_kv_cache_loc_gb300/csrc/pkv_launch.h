@@ -62,6 +62,13 @@ struct DecodeParams {
     // cache write before it; it reads metadata, slot indices and q at once
     // and waits (griddepcontrol.wait) before its first K/V row read.
     int32_t pdl;
+    // Page-table addressing (page_size > 0): position j of request row r is
+    // slot req_to_page[r * max_pages + j / page_size] * page_size +
+    // j % page_size, with pages < n_pages; req_to_token is not read.
+    const int32_t *req_to_page;
+    int32_t max_pages;
+    int32_t page_size;
+    int64_t n_pages;
 };
 
 // Ragged causal prefill.

@@ -148,6 +148,30 @@ def paged_decode(cache: KVCache, layer_id: int, q: torch.Tensor, o: Optional[tor
     return o
 
 
+def paged_decode_pages(cache: KVCache, layer_id: int, req_to_page: torch.Tensor, page_size: int,
+                       q: torch.Tensor, o: Optional[torch.Tensor] = None,
+                       sm_scale: Optional[float] = None, workspace: Optional[Workspace] = None,
+                       stream=None) -> torch.Tensor:
+    """paged_decode through a page table: position j of request row r reads
+    slot req_to_page[r, j // page_size] * page_size + j % page_size
+    (cache.req_to_token is not read)."""
+    dev = cache.device
+    if req_to_page.dim() != 2:
+        raise ValueError("req_to_page must be [num_reqs, max_pages]")
+    c = dataclasses.replace(cache, req_to_token=req_to_page).c_struct()
+    n_heads, head_dim = int(q.shape[1]), int(q.shape[2])
+    if o is None:
+        o = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(head_dim) if sm_scale is None else float(sm_scale)
+    rc = _lib.load().pkv_paged_decode_pages(ctypes.byref(c), layer_id, c.req_to_token,
+                                            int(req_to_page.shape[1]), int(page_size),
+                                            _need(q, "q", cache.k_buffer.dtype, dev),
+                                            _need(o, "o", cache.k_buffer.dtype, dev), n_heads, scale,
+                                            _ws(workspace), _stream(stream, dev))
+    check(rc, "pkv_paged_decode_pages")
+    return o
+
+
 def decode_step(cache: KVCache, layer_id: int, k_new: torch.Tensor, v_new: torch.Tensor,
                 q: torch.Tensor, o: Optional[torch.Tensor] = None,
                 sm_scale: Optional[float] = None, workspace: Optional[Workspace] = None,

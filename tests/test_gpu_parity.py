@@ -500,6 +500,63 @@ def test_decode_step_replays_in_a_cuda_graph():
     assert_close(f64(o), oracle_decode(case), "bf16", "step graph replay, new rows")
 
 
+def page_table(case):
+    """req_to_page of a case whose slots come in pages of page_size
+    consecutive slots (checked against req_to_token)."""
+    ps = case.page_size
+    r2t = case.req_to_token
+    n_cols = -(-r2t.shape[1] // ps)
+    table = np.zeros((r2t.shape[0], n_cols), np.int32)
+    table[:, :] = r2t[:, ::ps] // ps
+    for b in range(case.batch):
+        r, n = int(case.req_pool_indices[b]), int(case.seq_lens[b])
+        j = np.arange(n)
+        assert np.array_equal(r2t[r, :n], table[r, j // ps] * ps + j % ps)
+    return table
+
+
+def test_prefix_shared_decode_through_the_page_table():
+    """The prefix-shared workload (page_size 16) through req_to_page: equal to
+    the oracle, and bit-identical to the decode through req_to_token."""
+    case = W.prefix_shared_decode()
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    table = torch.from_numpy(page_table(case)).cuda()
+    o = pkv.paged_decode_pages(cache, case.layer_id, table, case.page_size, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "page table")
+    assert torch.equal(o, pkv.paged_decode(cache, case.layer_id, q, workspace=ws))
+
+
+@pytest.mark.parametrize("heads,hk,d,ps,indptr", [(16, 4, 128, 8, False), (8, 8, 64, 4, True),
+                                                 (32, 8, 128, 32, False)])
+def test_page_table_variants(heads, hk, d, ps, indptr):
+    """Page sizes 4..32, kv heads 4 or 8, head_dim 64 or 128, the balanced and
+    the chunked plans; ragged lengths that end inside a page."""
+    kv = [1, 15, 16, 17, 130, 700, 1023]
+    case = W.make_case("pages", mode="decode", dtype="bf16", n_layers=2, layer_id=1, size=8192,
+                       n_heads=heads, n_kv_heads=hk, head_dim=d, kv_lens=kv, page_size=ps, seed=31)
+    cache, q = prepare(case)
+    if not indptr:
+        cache.kv_indptr = None
+    ws = ws_for(case, splits=64)
+    table = torch.from_numpy(page_table(case)).cuda()
+    o = pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", f"pages ps={ps}")
+
+
+def test_page_index_outside_the_pool_is_reported():
+    case = W.make_case("pbad", mode="decode", dtype="bf16", n_layers=1, layer_id=0, size=1024,
+                       n_heads=8, n_kv_heads=8, head_dim=128, kv_lens=[40, 70], page_size=16, seed=5)
+    cache, q = prepare(case)
+    table = page_table(case)
+    table[case.req_pool_indices[1], 2] = 1024 // 16 + 3
+    pkv.paged_decode_pages(cache, 0, torch.from_numpy(table).cuda(), 16, q, workspace=ws_for(case))
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX and detail == 1024 // 16 + 3
+
+
 def test_decode_on_slot_maps_from_the_page_pool():
     """req_to_token rows produced by the host allocator after churn (shared
     prefixes reused from the prefix cache, freed and evicted pages, decode
