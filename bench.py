@@ -442,26 +442,42 @@ def run_pkv(args):
 
 def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of q, k_new, v_new and the per-step metadata, decode_step
-    (kv_write + paged_decode), D2H of o, all inside the events."""
-    from paged_kv_cache_loc_gb300 import workloads as W
-    hq = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(case.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    meta = [torch.from_numpy(a).pin_memory() for a in (case.seq_lens, case.req_pool_indices,
-                                                       case.out_cache_loc, case.kv_indptr)]
-    ho = torch.empty(hq.shape, dtype=torch.bfloat16).pin_memory()
-    dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (hq, hk, hv))
-    dmeta = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in meta]
-    do = torch.empty(hq.shape, dtype=torch.bfloat16, device=dev)
+    memory, packed the way a serving loop sends them: q, k_new, v_new and the
+    per-step metadata in one pinned buffer, one host-to-device copy, the step
+    call (decode_step) on views of the device copy, one device-to-host copy of
+    o -- all inside the events."""
+    parts = [np.ascontiguousarray(a) for a in (case.q, case.k_new, case.v_new, case.seq_lens,
+                                               case.req_pool_indices, case.out_cache_loc,
+                                               case.kv_indptr)]
+    offs, total = [], 0
+    for a in parts:   # 256-byte aligned fields
+        offs.append(total)
+        total += (a.nbytes + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    hb = host.numpy()
+    for a, off in zip(parts, offs):
+        hb[off: off + a.nbytes] = a.view(np.uint8).reshape(-1)
+    devbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(i, dtype, shape):
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        return devbuf[offs[i]: offs[i] + n].view(dtype).view(shape)
+
+    bf = torch.bfloat16
+    dq = view(0, bf, case.q.shape)
+    dk = view(1, bf, case.k_new.shape)
+    dv = view(2, bf, case.v_new.shape)
     c = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
-                    req_to_token=cache.req_to_token, req_pool_indices=dmeta[1],
-                    seq_lens=dmeta[0], out_cache_loc=dmeta[2], kv_indptr=dmeta[3],
-                    max_len=case.max_len)
+                    req_to_token=cache.req_to_token,
+                    req_pool_indices=view(4, torch.int32, case.req_pool_indices.shape),
+                    seq_lens=view(3, torch.int32, case.seq_lens.shape),
+                    out_cache_loc=view(5, torch.int32, case.out_cache_loc.shape),
+                    kv_indptr=view(6, torch.int32, case.kv_indptr.shape), max_len=case.max_len)
+    ho = torch.empty(case.q.shape, dtype=bf).pin_memory()
+    do = torch.empty(case.q.shape, dtype=bf, device=dev)
 
     def step():
-        for h, d in zip([hq, hk, hv] + meta, [dq, dk, dv] + dmeta):
-            d.copy_(h, non_blocking=True)
+        devbuf.copy_(host, non_blocking=True)
         if chunk == 0:
             pkv.decode_step(c, case.layer_id, dk, dv, dq, do, workspace=ws, stream=stream)
         else:
@@ -473,13 +489,15 @@ def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     with torch.cuda.stream(stream):
         ms, _ = timed(torch, stream, step, n, 5, flush)
     assert torch.equal(ho, do.cpu())
-    h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + meta)
+    h2d = total
     d2h = ho.numel() * ho.element_size()
     b = decode_bytes(case) + kv_write_bytes(case)
     t = statistics.mean(ms)
     return {"value": round(b / (t * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(t, 5),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "path": "pinned host -> device copies, public API (ctypes) calls, device -> pinned host"}
+            "path": ("one pinned host -> device copy of the packed step inputs (q, k_new, v_new, "
+                     "seq_lens, req_pool_indices, out_cache_loc, kv_indptr), the public API call, "
+                     "device -> pinned host copy of o")}
 
 
 def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
