@@ -105,6 +105,27 @@ def dist_info():
     return rank, world, local
 
 
+def rank_seed(rank: int) -> int:
+    """Seed of a rank's copy of the workload: the same shapes on every rank
+    (weak scaling), different values."""
+    return 1002 + 100 * rank
+
+
+def job_step_ms(torch, local_ms: float, dev) -> float:
+    """The job's step time: the slowest rank's (max over ranks)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_ms
+    t = torch.tensor([local_ms], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value_gbs(world: int, bytes_per_rank_step: float, job_ms: float) -> float:
+    """Whole-job throughput: the bytes every rank processed per step, over the job's step time."""
+    return world * bytes_per_rank_step / (job_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -329,7 +350,7 @@ def run_pkv(args):
     flush = make_l2_flush(torch, dev)
 
     # ---- the workload: batched GQA decode -------------------------------
-    case = W.batched_decode(seed=1002 + 100 * rank)
+    case = W.batched_decode(seed=rank_seed(rank))
     cache, q, kn, vn = W.upload(case, dev)
     o = torch.empty_like(q)
     ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024, device=dev)
@@ -375,12 +396,8 @@ def run_pkv(args):
     ms_decode = statistics.mean(parts[1])
     b_dec = decode_bytes(case)
     b_wr = kv_write_bytes(case)
-    total_ms = ms_step
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * (b_dec + b_wr) / (total_ms * 1e-3) / 1e9
+    total_ms = job_step_ms(torch, ms_step, dev)
+    value = job_value_gbs(world, b_dec + b_wr, total_ms)
 
     achieved = b_dec / (ms_decode * 1e-3) / 1e9
     roofline = {
