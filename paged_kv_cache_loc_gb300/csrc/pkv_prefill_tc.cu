@@ -23,9 +23,9 @@
 //    each of 8 tcgen05.mma (M=128, N=128, K=16), so the tensor core works on
 //    one query tile while the softmax runs on the other;
 //  - softmax warps 0..7: warps w and w+4 share TMEM lanes 32(w%4).. and take
-//    one 64-column half of each row.  A thread reads its scores of S_X(j) in
-//    two 32-column passes (the row maximum, exchanged with the other half
-//    through shared memory and a named barrier; then P), keeps a running
+//    one 64-column half of each row.  A thread reads its 64 scores of S_X(j)
+//    into registers once, exchanges its half's maximum with the other half
+//    through shared memory and a named barrier, keeps a running
 //    maximum that is only raised when the tile maximum exceeds it by more
 //    than 2^8 (then its half of O_X is rescaled in TMEM -- P.V_X(j-1) is
 //    complete, as it was issued before S_X(j)), and stores P = 2^(s - m) as
@@ -130,6 +130,19 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane; the wait is in the
+// same asm block, so the values exist only once the load has completed
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 // 32 consecutive fp32 columns of this thread's TMEM lane (load and wait)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -176,13 +189,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
-__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
 }
-
 template <int G>
 __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams p) {
     using bf16 = __nv_bfloat16;
@@ -426,18 +436,19 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 fence_after();
                 const uint32_t tS = tmem + X * 256 + lane_off + hc * 64;
                 const int jt = j * kTok + hc * 64;
-                // pass 1: the row maximum of this half
+                // this half's 64 scores, read once; masked only near the diagonal
+                float sv[64];
+                tmem_ld64(tS, sv);
+                if (jt + 63 > lim[X]) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (jt + i > lim[X]) sv[i] = -INFINITY;
+                }
                 float mx[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float v[32];
-                    tmem_ld32(tS + c * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        mx[i & 7] = fmaxf(mx[i & 7], jt + c * 32 + i > lim[X] ? -INFINITY : v[i]);
-                }
+                for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
                 float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;   // -inf stays -inf
                 float *red = s_red + (X * 2 + (j & 1)) * 2 * kRows;
@@ -453,8 +464,8 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 if (__any_sync(0xffffffffu, touch_o)) {
                     const float f = touch_o ? alpha : 1.f;
                     const uint32_t tO = tmem + X * 256 + 128 + lane_off + hc * 64;
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll 1
+                    for (int h2 = 0; h2 < 2; ++h2) {   // one 32-column piece at a time: sv stays live
                         float v[32];
                         tmem_ld32(tO + h2 * 32, v);
 #pragma unroll
@@ -466,27 +477,24 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                     l_part[X] *= alpha;
                     m_run[X] = mt;
                 }
-                // pass 2: P = 2^(s - m) as bf16 pairs over the columns just read;
-                // a row with nothing visible yet keeps P = 0 (reference -inf,
-                // fma(v, scale, -inf) = -inf for finite or -inf v)
+                // P = 2^(s - m) as bf16 pairs over the first 32 of this half's S
+                // columns (already read); a row with nothing visible yet keeps
+                // P = 0 (reference -inf, fma(v, scale, -inf) = -inf for finite
+                // or -inf v)
                 const float neg_m = m_run[X] == -INFINITY ? -INFINITY : -m_run[X];
                 float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float v[32];
-                    tmem_ld32(tS + c * 32, v);
-                    uint32_t pk[16];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float s0 = jt + c * 32 + i > lim[X] ? -INFINITY : v[i];
-                        const float s1 = jt + c * 32 + i + 1 > lim[X] ? -INFINITY : v[i + 1];
-                        const float p0 = ex2_approx(fmaf(s0, sc, neg_m));
-                        const float p1 = ex2_approx(fmaf(s1, sc, neg_m));
+                    for (int i = 0; i < 16; i += 2) {
+                        const float p0 = ex2_approx(fmaf(sv[c * 16 + i], sc, neg_m));
+                        const float p1 = ex2_approx(fmaf(sv[c * 16 + i + 1], sc, neg_m));
                         ls[(i >> 1) & 7] += p0 + p1;
                         __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
                         pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
                     }
-                    tmem_st16u(tS + c * 16, pk);
+                    tmem_st8u(tS + c * 8, pk);
                 }
                 l_part[X] += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
