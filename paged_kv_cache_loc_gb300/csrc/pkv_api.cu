@@ -375,7 +375,7 @@ int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, c
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!no_write) {
-        rc = map_launch(pkv::launch_kv_write(wp, s));
+        rc = map_launch(pkv::launch_kv_write(wp, s, true));
         if (rc) return rc;
     }
     if (no_decode) return PKV_OK;

@@ -19,6 +19,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// kStep: the write of a decode step (launched with the shared-memory
+// carve-out at its maximum, see launch_kv_write); same code otherwise.
+template <bool kStep>
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams p) {
     // A decode split kernel launched as a programmatic dependent of this write
     // may start now: it reads metadata while the write runs and waits for this
@@ -134,24 +137,29 @@ inline unsigned grid_for(const KvWriteParams &p) {
 
 }  // namespace
 
-cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s) {
+cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s, bool step) {
     if (p.n_new == 0) return cudaSuccess;
-    // The write uses no shared memory.  With the carve-out at its shared
-    // maximum, the decode kernel that follows in a step (about 208 KB of
-    // shared memory per SM) fits beside it, and the SMs need no
-    // reconfiguration between the two.
+    if (!step) {
+        kv_write_kernel<false><<<grid_for(p), kThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    // The write uses no shared memory.  In a decode step, with the carve-out
+    // at its shared maximum, the decode kernel that follows (about 208 KB of
+    // shared memory per SM) fits beside it and the SMs need no
+    // reconfiguration between the two.  A standalone write keeps the default
+    // carve-out of whatever ran before it.
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        e = cudaFuncSetAttribute(kv_write_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(kv_write_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
-    kv_write_kernel<<<grid_for(p), kThreads, 0, s>>>(p);
+    kv_write_kernel<true><<<grid_for(p), kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -100,7 +100,8 @@ constexpr int kDecodeMaxSplits = 1024;  // merge kernel limit
 
 // Each returns cudaSuccess or the launch error.  Unsupported variants return
 // cudaErrorNotSupported and enqueue nothing.
-cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s);
+// step: the write of pkv_decode_step (see pkv_kv_write.cu)
+cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s, bool step = false);
 cudaError_t launch_rope_kv_write(const KvWriteParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int dtype, int head_dim, int group,
                           cudaStream_t s);
