@@ -13,13 +13,16 @@
 //
 // Two kernels share these building blocks:
 //  - decode_mma_kernel: one CTA per (split, kv head, entry), four warps each
-//    running its own cp.async ring over interleaved 16-token blocks; used
-//    when n_kv_heads does not divide 8;
+//    running its own cp.async ring over interleaved 16-token blocks (rows
+//    XOR-swizzled in shared memory); used when n_kv_heads does not divide 8;
 //  - decode_mma_allheads_kernel: one CTA reads whole slot rows of all kv
-//    heads (below), either per (split, entry) or over an exactly balanced
-//    partition of all tokens of the batch.
-// Rows are XOR-swizzled in shared memory so that ldmatrix is free of bank
-// conflicts; per-warp (m, l, O) are combined in shared memory at the end.
+//    heads (K rows by bulk copy, V rows by cp.async, rows padded by 16 bytes
+//    so ldmatrix is free of bank conflicts), either per (split, entry) or
+//    over an exactly balanced partition of all tokens of the batch.  With 8
+//    kv heads a CTA stages the slots of all its pieces at once and streams
+//    them through one ring (stream_pieces); otherwise piece by piece.
+// Slots come from req_to_token, or from a page table (slot_at).  The merge of
+// the balanced partition (decode_merge_balanced_kernel) is at the end.
 #include <atomic>
 
 #include "pkv_common.cuh"
