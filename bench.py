@@ -105,6 +105,16 @@ def dist_info():
     return rank, world, local
 
 
+def workload_config(case, world: int) -> dict:
+    """The workload description both arms report (the implementation adds its plan)."""
+    return {"workload": "batched GQA decode", "batch": case.batch, "n_heads": case.n_heads,
+            "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
+            "seq_lens": "uniform [512, 4096]", "total_kv_tokens": int(case.seq_lens.sum()),
+            "pool_slots": case.size, "n_layers": case.n_layers, "layer_id": case.layer_id,
+            "page_size": 1, "new_tokens_per_step": int(case.out_cache_loc.size),
+            "parallelism": f"replicas x{world}"}
+
+
 def rank_seed(rank: int) -> int:
     """Seed of a rank's copy of the workload: the same shapes on every rank
     (weak scaling), different values."""
@@ -424,13 +434,8 @@ def run_pkv(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) K/V/q, permuted slots)",
-        "config": {"workload": "batched GQA decode", "batch": case.batch, "n_heads": case.n_heads,
-                   "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
-                   "seq_lens": "uniform [512, 4096]", "total_kv_tokens": int(case.seq_lens.sum()),
-                   "pool_slots": case.size, "n_layers": case.n_layers, "layer_id": case.layer_id,
-                   "page_size": 1, "decode_plan": mode,
-                   "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(workload_config(case, world), decode_plan=mode,
+                       l2="flushed before every timed step (256 MB write, then 256 MB read)"),
         "decode_tokens_per_s": round(world * case.batch / (total_ms * 1e-3), 1),
         "attention_stack_tokens_per_s": round(world * case.batch / (case.n_layers * total_ms * 1e-3), 1),
         "kv_write_ms": round(ms_write, 5),
@@ -683,9 +688,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) K/V/q, permuted slots)",
-        "config": {"workload": "batched GQA decode", "batch": case.batch, "n_heads": case.n_heads,
-                   "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim,
-                   "seq_lens": "uniform [512, 4096]"},
+        "config": dict(workload_config(case, world), decode_plan="oracle: one plain pass per request",
+                       l2="host memory (the oracle runs on the host cores)"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "each step = one request's cache write + decode (all 32 heads), "
                                    "cycling through the 32 requests of the workload"},
