@@ -51,9 +51,57 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the prefill / long-context / e2e / cpu legs")
     ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="print decode KV GB/s over batch x context (uniform contexts) and exit")
     ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "kvwrite"],
                     help="run a few untimed calls of one kernel's case (for ncu) and exit")
     return ap.parse_args()
+
+
+DECODE_SWEEP = [(1, 16384), (8, 1024), (8, 4096), (8, 16384), (32, 1024), (32, 4096), (32, 16384),
+                (128, 1024), (128, 4096), (256, 1024), (256, 2048), (512, 512), (512, 1024),
+                (1100, 256)]
+
+
+def run_decode_sweep() -> None:
+    """Decode (automatic plan) over batch x uniform context, 32/8 heads, d=128,
+    bf16, permuted slots; L2 flushed before each call; one JSON line per point."""
+    import torch
+    import paged_kv_cache_loc_gb300 as pkv
+    from paged_kv_cache_loc_gb300 import build
+    from paged_kv_cache_loc_gb300 import workloads as W
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = make_l2_flush(torch, dev)
+    stream = torch.cuda.Stream(device=dev)
+    peaks = measured_peaks()
+    for batch, ctx in DECODE_SWEEP:
+        tokens = batch * ctx
+        size = max(65536, ((tokens + batch + 4095) // 4096) * 4096)
+        case = W.make_case("sweep", mode="decode", dtype="bf16", n_layers=1, layer_id=0, size=size,
+                           n_heads=32, n_kv_heads=8, head_dim=128, kv_lens=[ctx] * batch,
+                           seed=batch + ctx)
+        cache, q, kn, vn = W.upload(case, dev)
+        pkv.kv_write(cache, 0, kn, vn)
+        ws = pkv.Workspace(batch, 32, 128, max(2, -(-(152 + batch) // batch)), device=dev)
+        chunk, parts = pkv.decode_plan(cache, 32, ws)
+        o = torch.empty_like(q)
+        with torch.cuda.stream(stream):
+            ms, _ = timed(torch, stream, lambda: pkv.paged_decode(cache, 0, q, o, workspace=ws,
+                                                                stream=stream), 30, 5, flush)
+        st, detail = pkv.last_device_error(stream, dev)
+        if st != 0:
+            raise RuntimeError(f"device error word set in the sweep (detail {detail})")
+        t = statistics.median(ms)
+        b = decode_bytes(case)
+        print(json.dumps({"batch": batch, "context": ctx, "us_per_decode": round(t * 1e3, 1),
+                          "kv_gbs": round(b / (t * 1e-3) / 1e9, 1),
+                          "frac_of_hbm_peak": round(b / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "plan": f"balanced: {parts} CTAs" if chunk == 0 else f"chunked: {chunk}"}),
+              flush=True)
+        del cache, q, kn, vn, ws, o, case
+        torch.cuda.empty_cache()
 
 
 def run_profile_case(which: str) -> None:
@@ -700,7 +748,9 @@ def run_reference(args):
 
 def main():
     args = parse_args()
-    if args.profile_case:
+    if args.decode_sweep:
+        run_decode_sweep()
+    elif args.profile_case:
         run_profile_case(args.profile_case)
     elif args.impl == "reference":
         run_reference(args)
