@@ -369,8 +369,9 @@ def test_workspace_too_small_is_rejected():
     assert_close(f64(o), oracle_decode(case), "bf16", "2-split plan")
 
 
-def test_decode_step_replays_in_a_cuda_graph():
-    """kv_write + decode captured once, replayed with metadata updated in place."""
+def test_write_then_chunked_decode_replays_in_a_cuda_graph():
+    """kv_write + decode (fixed 64-token splits) captured once, replayed with
+    metadata updated in place."""
     case = W.batched_decode(batch=8, lo=100, hi=700, size=16384, seed=515)
     cache, q, kn, vn = W.upload(case)
     ws = ws_for(case, splits=64)
