@@ -351,6 +351,18 @@ class DecodeStep:
                                                      self.s), "pkv_paged_decode")
 
 
+def graph_replay_ms(torch, stream, fn, steps, warmup, flush):
+    """Capture fn() once in a CUDA graph on `stream` and time its replays with
+    the L2 flushed before each (the flush stays outside the graph)."""
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    ms, _ = timed(torch, stream, g.replay, steps, warmup, flush)
+    return ms, g
+
+
 def make_l2_flush(torch, dev):
     """Evict L2 between timed steps: write a 256 MB buffer, then read another
     256 MB so that the dirty lines of the write are written back before the
@@ -498,6 +510,9 @@ def run_pkv(args):
 
     if not args.no_extras:
         out["e2e"] = e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev)
+        if chunk == 0:
+            out["graph_step"] = graph_step_leg(torch, step, stream, flush, args, b_dec + b_wr,
+                                               ms_step, peaks)
         out["long_context_b1"] = long_context_leg(torch, pkv, W, stream, flush, peaks, dev)
         out["prefix_shared_pages"] = prefix_shared_leg(torch, pkv, W, stream, flush, peaks, dev)
         out["prefill"] = prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev)
@@ -508,6 +523,20 @@ def run_pkv(args):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def graph_step_leg(torch, step, stream, flush, args, step_bytes, eager_ms, peaks):
+    """The decode step as a serving loop replays it: the pkv_decode_step call
+    captured once in a CUDA graph (its programmatic edge becomes a graph
+    edge), replayed with the L2 flushed before each replay."""
+    with torch.cuda.stream(stream):
+        ms, g = graph_replay_ms(torch, stream, step.fused, args.steps, args.warmup, flush)
+    t = statistics.mean(ms)
+    del g
+    return {"us_per_step": round(t * 1e3, 2), "kv_gbs": round(step_bytes / (t * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(step_bytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "eager_us_per_step": round(eager_ms * 1e3, 2),
+            "what": "pkv_decode_step captured in a CUDA graph, replayed; L2 flushed before each replay"}
 
 
 def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
@@ -585,17 +614,25 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
             ms, _ = timed(torch, stream,
                           lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
                                                    stream=stream), 100, 10, flush)
+            gms, g = graph_replay_ms(
+                torch, stream, lambda: pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws,
+                                                        stream=stream), 100, 10, flush)
+            del g
         t = statistics.median(ms)
+        tg = statistics.median(gms)
         b = decode_bytes(case)
         gbs = b / (t * 1e-3) / 1e9
         sweep.append({"context": ctx, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
                       "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                      "graph_us_per_decode": round(tg * 1e3, 2),
+                      "graph_frac_of_hbm_peak": round(b / (tg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                       "decode_plan": (f"balanced: {n_splits} CTAs" if plan_chunk == 0
                                       else f"chunked: {plan_chunk}-token splits"),
                       "algorithmic_bytes": b})
         del cache, q, kn, vn, ws, o
     out = dict(sweep[-1])
-    out["sweep"] = [{k: s[k] for k in ("context", "us_per_decode", "kv_gbs", "frac_of_hbm_peak")}
+    out["sweep"] = [{k: s[k] for k in ("context", "us_per_decode", "kv_gbs", "frac_of_hbm_peak",
+                                       "graph_us_per_decode")}
                     for s in sweep]
     return out
 
