@@ -203,10 +203,24 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
  * Requires c->size to be a multiple of page_size.  Supported: bf16,
  * head_dim 64 or 128, G and n_kv_heads in {1, 2, 4, 8}.  A page index
  * outside [0, size / page_size) is a device-data error.
+ *
+ * shared_pages: the caller's statement that the first shared_pages pages of
+ * every row of the batch are the same pages (a prefix shared by all
+ * requests, "KVCache System" prefix cache hits); 0 states nothing.  It does
+ * not change the result: with 8 kv heads, at least 64 shared positions
+ * (shared_pages * page_size), batch >= 2 and room in the workspace it lets
+ * the decode read each shared K/V row once per group of 16 / G requests
+ * instead of once per request, and merge the two parts (the workspace then
+ * holds (CTAs + batch) x n_heads rows plus (CTAs + ceil(batch / (16 / G)))
+ * x (16 / G) x n_heads more); otherwise it is ignored.  Every seq_len must
+ * be >= shared_pages * page_size; a shorter context, or a row whose leading
+ * pages differ from its group's, is a device-data error.  shared_pages < 0,
+ * or shared positions beyond c->max_len, returns PKV_ERR_ARG.
  */
 int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t *req_to_page,
-                           int32_t max_pages, int32_t page_size, const void *q, void *o,
-                           int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
+                           int32_t max_pages, int32_t page_size, int32_t shared_pages,
+                           const void *q, void *o, int32_t n_heads, float sm_scale,
+                           const pkv_workspace *ws, void *stream);
 
 /*
  * One decode step of a layer ("Attention Backend": the new tokens' K/V go

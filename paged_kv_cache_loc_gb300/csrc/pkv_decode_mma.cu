@@ -103,6 +103,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
     return false;
 }
+// Partial stores with L2 evict_last priority: the merge reads the partials
+// right after the split, whose K/V stream (usually larger than L2) would
+// otherwise push the early ones out to DRAM.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_keep(float *addr, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(addr), "f"(v), "l"(pol) : "memory");
+}
+
 // Wait for the grid this one depends on programmatically (the cache write
 // of a decode step) to complete and its writes to become visible.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
@@ -453,6 +465,109 @@ __device__ __forceinline__ int part_of(long long t, long long T, int P) {
     return static_cast<int>(c < P - 1 ? c : P - 1);
 }
 
+// Shared-prefix mode: the n_parts CTAs divide into the group role (p_sh CTAs
+// over the group space [0, n_groups * shared_len)) and the private role (the
+// rest, over the private space [0, T - batch * shared_len)) in proportion to
+// the two token counts (group tokens weighted 9/8), with at least ceil(group space / 1024) group CTAs so
+// that none stages more than 1024 positions.  The split and merge kernels
+// derive it alike from T = kv_indptr[batch]; *_e are the CTAs that hold
+// tokens (a role with fewer tokens than CTAs leaves the rest idle).
+struct SharedRoles {
+    long long t_sh, t_pr;
+    int p_sh, p_pr, p_sh_e, p_pr_e;
+};
+__device__ __forceinline__ SharedRoles shared_roles(const DecodeParams &p, long long T) {
+    SharedRoles r;
+    r.t_sh = static_cast<long long>(p.n_groups) * p.shared_len;
+    r.t_pr = T - static_cast<long long>(p.batch) * p.shared_len;
+    const int P = p.n_parts;
+    if (r.t_pr <= 0) {
+        r.p_sh = P;
+        r.p_pr = 0;
+    } else {
+        // a group token costs ~9/8 of a private one (16 query columns, not 8)
+        const long long w_sh = 9 * r.t_sh, tot = w_sh + 8 * r.t_pr;
+        long long psh = (static_cast<long long>(P) * w_sh + tot / 2) / tot;
+        psh = max(psh, (r.t_sh + 1023) / 1024);
+        psh = min(psh, static_cast<long long>(P - 1));
+        r.p_sh = static_cast<int>(psh);
+        r.p_pr = P - r.p_sh;
+    }
+    r.p_sh_e = static_cast<int>(min(static_cast<long long>(r.p_sh), r.t_sh));
+    r.p_pr_e = r.t_pr > 0 ? static_cast<int>(min(static_cast<long long>(r.p_pr), r.t_pr)) : 0;
+    return r;
+}
+
+// The raw table entry behind position j of request row r (the page id, or
+// the slot with req_to_token); two rows share position j's slot iff these
+// are equal.
+__device__ __forceinline__ int table_entry(const DecodeParams &p, int r, int j) {
+    if (p.page_size > 0)
+        return __ldg(p.req_to_page + static_cast<int64_t>(r) * p.max_pages + j / p.page_size);
+    return __ldg(p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len + j);
+}
+
+// block_math over two 8-column tiles of the score block (16 query columns):
+// each K and V^T fragment is loaded from shared memory once and used by both
+// tiles.  m / l hold, per tile, the running max and sum of this lane's two
+// columns.
+template <int D>
+__device__ __forceinline__ void block_math2(const __nv_bfloat16 *kt, const __nv_bfloat16 *vt,
+                                            int pitch, int valid, int lane, float scale_log2,
+                                            const uint32_t (&qb)[2][D / 16][2],
+                                            float (&o_acc)[2][D / 16][4], float (&m)[2][2],
+                                            float (&l)[2][2]) {
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, kt + (lane & 15) * pitch + (2 * ks + (lane >> 4)) * 8);
+        mma16816(s[0], a, qb[0][ks][0], qb[0][ks][1]);
+        mma16816(s[1], a, qb[1][ks][0], qb[1][ks][1]);
+    }
+    const int tA = lane >> 2, tB = tA + 8;
+    uint32_t pb[2][2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        s[t][0] = tA < valid ? s[t][0] * scale_log2 : -INFINITY;
+        s[t][1] = tA < valid ? s[t][1] * scale_log2 : -INFINITY;
+        s[t][2] = tB < valid ? s[t][2] * scale_log2 : -INFINITY;
+        s[t][3] = tB < valid ? s[t][3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(s[t][0], s[t][2]), mx1 = fmaxf(s[t][1], s[t][3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
+        const float al0 = exp2f(m[t][0] - mn0), al1 = exp2f(m[t][1] - mn1);
+        m[t][0] = mn0;
+        m[t][1] = mn1;
+        const float p0 = exp2f(s[t][0] - mn0), p1 = exp2f(s[t][1] - mn1);
+        const float p2 = exp2f(s[t][2] - mn0), p3 = exp2f(s[t][3] - mn1);
+        l[t][0] = l[t][0] * al0 + p0 + p2;
+        l[t][1] = l[t][1] * al1 + p1 + p3;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                o_acc[t][i][0] *= al0;
+                o_acc[t][i][1] *= al1;
+                o_acc[t][i][2] *= al0;
+                o_acc[t][i][3] *= al1;
+            }
+        }
+        pb[t][0] = movmatrix_t(pack_bf16(p0, p1));
+        pb[t][1] = movmatrix_t(pack_bf16(p2, p3));
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, vt + ((lane & 7) + ((lane >> 4) << 3)) * pitch + (2 * mt + ((lane >> 3) & 1)) * 8);
+        mma16816(o_acc[0][mt], a, pb[0][0], pb[0][1]);
+        mma16816(o_acc[1][mt], a, pb[1][0], pb[1][1]);
+    }
+}
+
 // Balanced-mode CTA c with one warp per kv head (8 kv heads), when its range
 // [t0, t1) holds at most kMaxPieces entry pieces and their slots fit the slot
 // array after rounding each piece up to whole 16-token stages.  Then:
@@ -545,7 +660,7 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
             s_s0[cbase] = static_cast<int>(max(lo, t0) - lo);
             s_len[cbase] = len;
             s_off[cbase] = pbase;
-            s_direct[cbase] = lo >= t0 && hi <= t1;
+            s_direct[cbase] = lo >= t0 && hi <= t1 && p.shared_len == 0;
             ++cbase;
             pbase += (len + 15) & ~15;
         }
@@ -577,7 +692,7 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
             if (s_off[mid] <= j) a = mid; else z = mid - 1;
         }
         const int pos = min(j - s_off[a], s_len[a] - 1);
-        slots[j] = slot_at(p, s_r[a], s_s0[a] + pos);
+        slots[j] = slot_at(p, s_r[a], p.shared_len + s_s0[a] + pos);
     }
     __syncthreads();
     if (p.pdl) griddep_wait();   // K/V rows may come from the cache write before this kernel
@@ -666,26 +781,27 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
         } else {
             const int64_t row = (static_cast<int64_t>(c) + b) * p.n_heads + hw * G;
             float *op = p.o_part + row * D;
+            const uint64_t pol = l2_keep_policy();
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 const int d = mt * 16 + (lane >> 2);
                 if (h0 < G) {
-                    op[h0 * D + d] = o_acc[mt][0] * i0;
-                    op[h0 * D + d + 8] = o_acc[mt][2] * i0;
+                    st_keep(op + h0 * D + d, o_acc[mt][0] * i0, pol);
+                    st_keep(op + h0 * D + d + 8, o_acc[mt][2] * i0, pol);
                 }
                 if (h1 < G) {
-                    op[h1 * D + d] = o_acc[mt][1] * i1;
-                    op[h1 * D + d + 8] = o_acc[mt][3] * i1;
+                    st_keep(op + h1 * D + d, o_acc[mt][1] * i1, pol);
+                    st_keep(op + h1 * D + d + 8, o_acc[mt][3] * i1, pol);
                 }
             }
             if (lane < 4) {
                 if (h0 < G) {
-                    p.ml_part[(row + h0) * 2] = m0;
-                    p.ml_part[(row + h0) * 2 + 1] = l0;
+                    st_keep(p.ml_part + (row + h0) * 2, m0, pol);
+                    st_keep(p.ml_part + (row + h0) * 2 + 1, l0, pol);
                 }
                 if (h1 < G) {
-                    p.ml_part[(row + h1) * 2] = m1;
-                    p.ml_part[(row + h1) * 2 + 1] = l1;
+                    st_keep(p.ml_part + (row + h1) * 2, m1, pol);
+                    st_keep(p.ml_part + (row + h1) * 2 + 1, l1, pol);
                 }
             }
         }
@@ -705,7 +821,222 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
     return true;
 }
 
-template <int D, int G, int HK>
+// Group role of the shared-prefix mode (one warp per kv head, 8 kv heads).
+// CTA cs covers [t0, t1) of the group space, where group gi owns
+// [gi * Ts, gi * Ts + Ts): the shared positions of entries gi * R ..
+// gi * R + R - 1 (R = 16 / G).  Each group piece is read once for all its
+// entries: column col = 8 t + (lane >> 2) of n-tile t is entry
+// gi * R + col / G, head hw * G + col % G (columns past the batch hold
+// q = 0 and are not written).  All slot indices are staged at once, from
+// the group's first entry, each piece padded to whole 16-token stages; every
+// other member's table entries over the piece are compared with the
+// first's and a mismatch is recorded (the shared-prefix claim was false).
+// Each piece ends in one partial per (member, head).
+template <int D, int G>
+__device__ __forceinline__ void stream_group(const DecodeParams &p, int cs, long long t0, long long t1,
+                                             int *slots, uint64_t *bars, __nv_bfloat16 *ring) {
+    using C = AllHeadsCfg<D, 8>;
+    using bf16 = __nv_bfloat16;
+    constexpr int NT = C::kNTAH, S = C::kStages, R = 16 / G;
+    constexpr int kMaxGroupPieces = 24;
+    static_assert(C::kTS == 16, "one 16-token block per warp and stage");
+    __shared__ int g_gi[kMaxGroupPieces], g_s0[kMaxGroupPieces], g_len[kMaxGroupPieces],
+        g_off[kMaxGroupPieces], g_r[kMaxGroupPieces];
+    __shared__ int g_n, g_total, g_abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Ts = p.shared_len;
+
+    if (tid == 0) {
+        int n = 0, off = 0;
+        for (long long gi = t0 / Ts; gi * Ts < t1; ++gi) {
+            const long long lo = gi * Ts;
+            const int s0 = static_cast<int>(max(t0, lo) - lo);
+            const int len = static_cast<int>(min(t1, lo + Ts) - lo) - s0;
+            if (len <= 0) continue;
+            if (n == kMaxGroupPieces || off + ((len + 15) & ~15) > kDecodeMaxChunk) {
+                record_error(p.err, -4000 - cs);   // the host keeps ranges within these bounds
+                break;
+            }
+            int r = __ldg(p.req_pool_indices + gi * R);
+            if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+                record_error(p.err, r);
+                r = 0;
+            }
+            g_gi[n] = static_cast<int>(gi);
+            g_s0[n] = s0;
+            g_len[n] = len;
+            g_off[n] = off;
+            g_r[n] = r;
+            off += (len + 15) & ~15;
+            ++n;
+        }
+        g_n = n;
+        g_total = off;
+        g_abort = 0;
+    }
+    __syncthreads();
+    const int n_pieces = g_n, total = g_total;
+    if (n_pieces == 0) return;
+
+    const int hw = warp;   // this warp's kv head
+    auto load_q = [&](int pc, uint32_t (&qr)[2][D / 16][2]) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int col = 8 * t + (lane >> 2);
+            const int b = g_gi[pc] * R + col / G;
+            const bool ok = b < p.batch;
+            const bf16 *qrow = static_cast<const bf16 *>(p.q) +
+                               (static_cast<int64_t>(ok ? b : 0) * p.n_heads + hw * G + col % G) * D +
+                               2 * (lane & 3);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qr[t][ks][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16) : 0u;
+                qr[t][ks][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8) : 0u;
+            }
+        }
+    };
+    uint32_t qb[2][D / 16][2];
+    load_q(0, qb);
+
+    // stage every slot index (padding rows repeat the piece's last slot)
+    for (int j = tid; j < total; j += NT) {
+        int a = 0;
+        while (a + 1 < n_pieces && g_off[a + 1] <= j) ++a;
+        const int pos = min(j - g_off[a], g_len[a] - 1);
+        slots[j] = slot_at(p, g_r[a], g_s0[a] + pos);
+    }
+    __syncthreads();
+    if (p.pdl) griddep_wait();   // K/V rows may come from the cache write before this kernel
+
+    const int64_t slot_stride = static_cast<int64_t>(8) * D;
+    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + p.layer_row0 * slot_stride;
+    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + p.layer_row0 * slot_stride;
+    const int nst = total / 16;
+    auto issue = [&](int k) {
+        const int st = k % S;
+        bf16 *dst0 = ring + st * C::kStageElems;
+        const int *sl = slots + k * 16;
+        if (warp == 0) {
+            const uint32_t bar = smem_u32(bars + st);
+            if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(16 * C::kRowBytes));
+            __syncwarp();
+            if (lane < 16)
+                bulk_g2s(smem_u32(dst0 + lane * C::kPitch), kbase + sl[lane] * slot_stride, C::kRowBytes, bar);
+        }
+        constexpr int kVChunks = C::kRowBytes / 16;
+        bf16 *vdst = dst0 + C::kPartElems;
+#pragma unroll
+        for (int i = tid; i < 16 * kVChunks; i += NT) {
+            const int t = i / kVChunks, ch = i - t * kVChunks;
+            cp_async16(vdst + t * C::kPitch + ch * 8, vbase + sl[t] * slot_stride + ch * 8);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        if (k < nst) issue(k);
+        else cp_async_commit();
+    }
+    // with the first stages in flight: the other members' table entries must
+    // equal the first member's wherever a new entry (page) starts
+    for (int j = tid; j < total; j += NT) {
+        int a = 0;
+        while (a + 1 < n_pieces && g_off[a + 1] <= j) ++a;
+        const int rel = j - g_off[a];
+        const int jp = g_s0[a] + rel;
+        if (rel >= g_len[a] || (p.page_size > 0 && jp % p.page_size != 0 && rel != 0)) continue;
+        const int lead = table_entry(p, g_r[a], jp);
+        for (int u = 1; u < R; ++u) {
+            const int b = g_gi[a] * R + u;
+            if (b >= p.batch) break;
+            const int r = __ldg(p.req_pool_indices + b);
+            if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+                record_error(p.err, r);
+                continue;
+            }
+            if (table_entry(p, r, jp) != lead) record_error(p.err, -3000 - b);
+        }
+    }
+
+    float o_acc[2][D / 16][4];
+    float m[2][2], l[2][2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) o_acc[t][i][0] = o_acc[t][i][1] = o_acc[t][i][2] = o_acc[t][i][3] = 0.f;
+        m[t][0] = m[t][1] = -INFINITY;
+        l[t][0] = l[t][1] = 0.f;
+    }
+    int pc = 0;
+    int pend = (g_off[0] + ((g_len[0] + 15) & ~15)) >> 4;
+    for (int k = 0; k < nst; ++k) {
+        cp_async_wait<S - 2>();
+        __syncthreads();
+        if (g_abort) break;   // CTA-uniform after the barrier
+        if (k + S - 1 < nst) issue(k + S - 1);
+        else cp_async_commit();
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bars + k % S), (k / S) & 1));
+        if (!ok) {
+            if (lane == 0) {
+                record_error(p.err, -1000 - k);
+                g_abort = 1;
+            }
+            continue;
+        }
+        const bf16 *kt = ring + (k % S) * C::kStageElems + hw * D;
+        block_math2<D>(kt, kt + C::kPartElems, C::kPitch, g_len[pc] - (k * 16 - g_off[pc]), lane,
+                       p.scale_log2, qb, o_acc, m, l);
+        if (k + 1 < pend) continue;
+
+        // piece pc is complete: one partial per (member, head) from registers
+        const int gi = g_gi[pc];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
+                l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
+            }
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const int col = 8 * t + 2 * (lane & 3) + x;
+                const int u = col / G;
+                if (gi * R + u >= p.batch) continue;
+                const int64_t unit = p.group_unit0 +
+                                     (static_cast<int64_t>(cs + gi) * R + u) * p.n_heads + hw * G + col % G;
+                float *op = p.o_part + unit * D;
+                const float inv = 1.f / l[t][x];
+                const uint64_t pol = l2_keep_policy();
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d = mt * 16 + (lane >> 2);
+                    st_keep(op + d, o_acc[t][mt][x] * inv, pol);
+                    st_keep(op + d + 8, o_acc[t][mt][2 + x] * inv, pol);
+                }
+                if (lane < 4) {
+                    st_keep(p.ml_part + unit * 2, m[t][x], pol);
+                    st_keep(p.ml_part + unit * 2 + 1, l[t][x], pol);
+                }
+            }
+        }
+        if (++pc == n_pieces) break;
+        pend = (g_off[pc] + ((g_len[pc] + 15) & ~15)) >> 4;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i)
+                o_acc[t][i][0] = o_acc[t][i][1] = o_acc[t][i][2] = o_acc[t][i][3] = 0.f;
+            m[t][0] = m[t][1] = -INFINITY;
+            l[t][0] = l[t][1] = 0.f;
+        }
+        load_q(pc, qb);
+    }
+    cp_async_wait<0>();
+}
+
+// kShared: the shared-prefix mode's instantiation (both roles); the plain
+// one holds no group-role code, so its register budget is its own.
+template <int D, int G, int HK, bool kShared>
 __global__ void __launch_bounds__(AllHeadsCfg<D, HK>::kNTAH, 1)
 decode_mma_allheads_kernel(const DecodeParams p) {
     using C = AllHeadsCfg<D, HK>;
@@ -917,7 +1248,7 @@ decode_mma_allheads_kernel(const DecodeParams p) {
     }
 
     // balanced partition of [0, T)
-    const int c = blockIdx.x;
+    int c = blockIdx.x;
     // With one warp per kv head (HK == NW) and at most KPT * NT entries, the
     // entries' metadata comes in one round trip together with T: thread i
     // holds entries [KPT i, KPT i + KPT).
@@ -935,28 +1266,62 @@ decode_mma_allheads_kernel(const DecodeParams p) {
     }
     const long long T = __ldg(p.kv_indptr + p.batch);
     if (T <= 0) return;
-    const int P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
+    // Shared-prefix mode (shared_len > 0; 8 kv heads): the first CTAs take
+    // the group role; the others partition the private space, where entry b
+    // holds [kv_indptr[b] - b Ts, kv_indptr[b + 1] - (b + 1) Ts) and offset
+    // x stands for position Ts + x.  Ts = 0: the plain balanced partition.
+    const long long Ts = kShared ? p.shared_len : 0;
+    long long Tw = T;
+    int P;
+    if (kShared) {
+        const SharedRoles ro = shared_roles(p, T);
+        if (c < ro.p_sh) {
+            if constexpr (kFast && kShared) {
+                if (c < ro.p_sh_e)
+                    stream_group<D, G>(p, c, ro.t_sh * c / ro.p_sh_e, ro.t_sh * (c + 1) / ro.p_sh_e, slots,
+                                       bars, ring);
+            }
+            return;
+        }
+        c -= ro.p_sh;
+        P = ro.p_pr_e;
+        Tw = ro.t_pr;
+#pragma unroll
+        for (int k = 0; k <= KPT; ++k)
+            if (e0 + k <= p.batch) ip[k] = static_cast<int>(ip[k] - (e0 + k) * Ts);
+#pragma unroll
+        for (int k = 0; k < KPT; ++k) {
+            if (e0 + k < p.batch && fast_batch) {
+                if (sq[k] < Ts) record_error(p.err, sq[k]);   // shorter than the shared prefix
+                sq[k] = static_cast<int>(sq[k] - Ts);
+            }
+        }
+    } else {
+        P = static_cast<int>(min(static_cast<long long>(p.n_parts), T));
+    }
     if (c >= P) return;
-    long long t0 = T * c / P;
-    const long long t1 = T * (c + 1) / P;
+    const int n_cap_w = static_cast<int>(n_cap - Ts);   // longest private range
+    long long t0 = Tw * c / P;
+    const long long t1 = Tw * (c + 1) / P;
 
     if constexpr (kFast) {
-        if (fast_batch && stream_pieces<D, G, KPT>(p, c, t0, t1, n_cap, ip, rq, sq, slots, bars, ring))
+        if (fast_batch && stream_pieces<D, G, KPT>(p, c, t0, t1, n_cap_w, ip, rq, sq, slots, bars, ring))
             return;
     }
 
     if (p.pdl) griddep_wait();   // piece-by-piece pass: wait before anything streams
+    auto ipw = [&](int e) { return static_cast<long long>(__ldg(p.kv_indptr + e)) - e * Ts; };
     int lo_b = 0, hi_b = p.batch - 1;   // first entry whose range ends after t0
     while (lo_b < hi_b) {
         const int mid = (lo_b + hi_b) >> 1;
-        if (__ldg(p.kv_indptr + mid + 1) > t0) hi_b = mid; else lo_b = mid + 1;
+        if (ipw(mid + 1) > t0) hi_b = mid; else lo_b = mid + 1;
     }
     for (int b = lo_b; b < p.batch && t0 < t1; ++b) {
-        const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+        const long long lo = ipw(b), hi = ipw(b + 1);
         if (hi <= t0) continue;
         const long long n = hi - lo;
         int r = __ldg(p.req_pool_indices + b);
-        if (n != __ldg(p.seq_lens + b) || n > n_cap || lo < 0 ||
+        if (n != __ldg(p.seq_lens + b) - Ts || n > n_cap_w || lo < 0 ||
             static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
             record_error(p.err, n);
             t0 = hi;
@@ -964,14 +1329,15 @@ decode_mma_allheads_kernel(const DecodeParams p) {
         }
         const int s0 = static_cast<int>(t0 - lo);
         const int s1 = static_cast<int>(min(t1, hi) - lo);
-        const bool whole = s0 == 0 && s1 == n;
-        segment(b, r, s0, s1, whole, (static_cast<int64_t>(c) + b) * p.n_heads, 1);
+        const bool whole = s0 == 0 && s1 == n && Ts == 0;
+        segment(b, r, static_cast<int>(s0 + Ts), static_cast<int>(s1 + Ts), whole,
+                (static_cast<int64_t>(c) + b) * p.n_heads, 1);
         t0 = lo + s1;
     }
 }
 
-template <int D, int G, int HK>
-cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
+template <int D, int G, int HK, bool kShared>
+cudaError_t run_allheads_k(const DecodeParams &p, cudaStream_t s) {
     using C = AllHeadsCfg<D, HK>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
@@ -979,7 +1345,7 @@ cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        e = cudaFuncSetAttribute(decode_mma_allheads_kernel<D, G, HK>,
+        e = cudaFuncSetAttribute(decode_mma_allheads_kernel<D, G, HK, kShared>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::kSmem));
         if (e != cudaSuccess) return e;
@@ -995,7 +1361,15 @@ cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_mma_allheads_kernel<D, G, HK>, p);
+    return cudaLaunchKernelEx(&cfg, decode_mma_allheads_kernel<D, G, HK, kShared>, p);
+}
+
+template <int D, int G, int HK>
+cudaError_t run_allheads(const DecodeParams &p, cudaStream_t s) {
+    if constexpr (HK == 8) {
+        if (p.shared_len > 0) return run_allheads_k<D, G, HK, true>(p, s);
+    }
+    return run_allheads_k<D, G, HK, false>(p, s);
 }
 
 template <int D, int G>
@@ -1131,6 +1505,117 @@ __global__ void __launch_bounds__(WPI > 8 ? 32 * WPI : 256) decode_merge_balance
     }
 }
 
+// Merge of the shared-prefix mode.  One warp per (entry b, head h): the
+// pieces are the private role's rows (c + b) for the CTAs c whose range
+// meets b's private positions, then the group role's units of member
+// u = b % R of group gi = b / R for the CTAs whose range meets the group's
+// [gi Ts, gi Ts + Ts).  Both lists follow from T and the shared_roles split,
+// as in the split kernel.  An entry shorter than the shared prefix, or with
+// metadata that does not fit the partition, is recorded and gets o = 0.
+template <int D>
+__global__ void __launch_bounds__(256, 4) decode_merge_shared_kernel(const DecodeParams p) {
+    constexpr int kCols = D / 4, kBatch = 6;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int item = blockIdx.x * 8 + warp;
+    if (item >= p.batch * p.n_heads) return;   // warp-uniform; no block barriers below
+    const int b = item / p.n_heads, h = item - b * p.n_heads;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.o) + static_cast<int64_t>(item) * D;
+    const long long Ts = p.shared_len;
+    const int R = p.group_reqs;
+    const long long T = __ldg(p.kv_indptr + p.batch);
+    const long long lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+    const long long n = hi - lo;
+    const int n_cap = min(p.max_len, p.max_ctx_len);
+    bool ok = T > 0 && n >= Ts && n == __ldg(p.seq_lens + b) && n <= n_cap && lo >= 0 && hi <= T;
+    int np_pr = 0, c_lo = 0, cs_lo = 0, np_sh = 0;
+    const int gi = b / R, u = b - (b / R) * R;
+    if (ok) {
+        const SharedRoles ro = shared_roles(p, T);
+        const long long plo = lo - b * Ts, phi = hi - (b + 1) * Ts;   // private range
+        if (phi > plo) {
+            ok = ro.p_pr_e > 0 && plo >= 0 && phi <= ro.t_pr;
+            if (ok) {
+                c_lo = part_of(plo, ro.t_pr, ro.p_pr_e);
+                np_pr = part_of(phi - 1, ro.t_pr, ro.p_pr_e) - c_lo + 1;
+            }
+        }
+        cs_lo = part_of(gi * Ts, ro.t_sh, ro.p_sh_e);
+        np_sh = part_of((gi + 1) * Ts - 1, ro.t_sh, ro.p_sh_e) - cs_lo + 1;
+    }
+    // the partials come from the split kernel, which may still run (the
+    // piece lists above need only the metadata)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (!ok) {
+        if (h == 0 && lane == 0) record_error(p.err, n);
+        for (int e = lane; e < D; e += 32) out[e] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const int np = np_pr + np_sh;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = 0; base < np; base += kBatch) {
+        float m[kBatch], l[kBatch];
+        float4 x[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+            x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int i = base + k;
+            if (i < np) {
+                const int64_t unit =
+                    i < np_pr ? (static_cast<int64_t>(c_lo) + i + b) * p.n_heads + h
+                              : p.group_unit0 +
+                                    ((static_cast<int64_t>(cs_lo) + (i - np_pr) + gi) * R + u) * p.n_heads + h;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ml_part) + unit);
+                m[k] = ml.x;
+                l[k] = ml.y;
+                if (lane < kCols) x[k] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + unit * D) + lane);
+            }
+        }
+        float nM = M;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) nM = fmaxf(nM, m[k]);
+        const float sc = exp2f(M - nM);
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        L *= sc;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float w = base + k < np ? l[k] * exp2f(m[k] - nM) : 0.f;
+            L += w;
+            acc.x = fmaf(w, x[k].x, acc.x);
+            acc.y = fmaf(w, x[k].y, acc.y);
+            acc.z = fmaf(w, x[k].z, acc.z);
+            acc.w = fmaf(w, x[k].w, acc.w);
+        }
+        M = nM;
+    }
+    if (lane < kCols) {
+        const float inv = 1.f / L;
+        *reinterpret_cast<__nv_bfloat162 *>(out + lane * 4) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(out + lane * 4 + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+}
+
+template <int D>
+cudaError_t launch_merge_shared(const DecodeParams &p, cudaStream_t s) {
+    const int items = p.batch * p.n_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((items + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_shared_kernel<D>, p);
+}
+
 template <int D, int WPI>
 cudaError_t launch_merge_wpi(const DecodeParams &p, cudaStream_t s) {
     const int items = p.batch * p.n_heads;
@@ -1150,6 +1635,7 @@ cudaError_t launch_merge_wpi(const DecodeParams &p, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_merge_d(const DecodeParams &p, cudaStream_t s) {
+    if (p.shared_len > 0) return launch_merge_shared<D>(p, s);
     // an entry has about (n_parts + batch) / batch pieces: up to 16 warps per
     // entry, each loading its pieces in one or two batches
     const int64_t per_entry = (static_cast<int64_t>(p.n_parts) + p.batch) / (p.batch > 0 ? p.batch : 1);

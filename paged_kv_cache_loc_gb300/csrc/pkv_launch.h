@@ -69,6 +69,19 @@ struct DecodeParams {
     int32_t max_pages;
     int32_t page_size;
     int64_t n_pages;
+    // Shared prefix (balanced mode, 8 kv heads): positions [0, shared_len)
+    // of every entry map to the same slots.  The first CTAs of the grid
+    // (the group role) stream that prefix once per group of group_reqs
+    // consecutive entries, the requests' heads side by side as the score
+    // block's 16 columns; the others (the private role) take the balanced
+    // partition of the positions [shared_len, seq_len) of all entries.  The
+    // group role's piece of group gi in its CTA cs is written for member u,
+    // head h to unit group_unit0 + ((cs + gi) * group_reqs + u) * n_heads + h
+    // of o_part / ml_part.  shared_len 0: off.
+    int32_t shared_len;
+    int32_t group_reqs;
+    int32_t n_groups;
+    int64_t group_unit0;
 };
 
 // Ragged causal prefill.

@@ -151,10 +151,12 @@ def paged_decode(cache: KVCache, layer_id: int, q: torch.Tensor, o: Optional[tor
 def paged_decode_pages(cache: KVCache, layer_id: int, req_to_page: torch.Tensor, page_size: int,
                        q: torch.Tensor, o: Optional[torch.Tensor] = None,
                        sm_scale: Optional[float] = None, workspace: Optional[Workspace] = None,
-                       stream=None) -> torch.Tensor:
+                       stream=None, shared_pages: int = 0) -> torch.Tensor:
     """paged_decode through a page table: position j of request row r reads
     slot req_to_page[r, j // page_size] * page_size + j % page_size
-    (cache.req_to_token is not read)."""
+    (cache.req_to_token is not read).  shared_pages states that the first
+    shared_pages pages of every row in the batch are the same pages; the
+    decode may then read those rows once per group of requests."""
     dev = cache.device
     if req_to_page.dim() != 2:
         raise ValueError("req_to_page must be [num_reqs, max_pages]")
@@ -165,6 +167,7 @@ def paged_decode_pages(cache: KVCache, layer_id: int, req_to_page: torch.Tensor,
     scale = 1.0 / math.sqrt(head_dim) if sm_scale is None else float(sm_scale)
     rc = _lib.load().pkv_paged_decode_pages(ctypes.byref(c), layer_id, c.req_to_token,
                                             int(req_to_page.shape[1]), int(page_size),
+                                            int(shared_pages),
                                             _need(q, "q", cache.k_buffer.dtype, dev),
                                             _need(o, "o", cache.k_buffer.dtype, dev), n_heads, scale,
                                             _ws(workspace), _stream(stream, dev))

@@ -165,17 +165,20 @@ def test_paged_decode_pages_rejects_bad_arguments(lib):
     c = fake_cache()
     T = ctypes.c_void_p(0xF00000)
     f = lib.pkv_paged_decode_pages
-    assert f(None, 2, T, 64, 16, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
-    assert f(ctypes.byref(c), 2, None, 64, 16, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
-    assert f(ctypes.byref(c), 2, T, 0, 16, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
-    assert f(ctypes.byref(c), 2, T, 64, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(None, 2, T, 64, 16, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, None, 64, 16, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, T, 0, 16, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, T, 64, 0, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
     # 1024 slots are not a whole number of 24-slot pages
-    assert f(ctypes.byref(c), 2, T, 64, 24, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, T, 64, 24, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
     # max_len 200 beyond the 12 * 16 positions the table covers
-    assert f(ctypes.byref(c), 2, T, 12, 16, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, T, 12, 16, 0, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
     # an empty batch: nothing to do, no CUDA call
-    assert f(ctypes.byref(fake_cache(batch=0)), 2, T, 64, 16, Q, O, 32, 0.1, None,
+    assert f(ctypes.byref(fake_cache(batch=0)), 2, T, 64, 16, 0, Q, O, 32, 0.1, None,
              None) == _lib.PKV_OK
+    # a negative shared prefix; shared positions beyond max_len (13 * 16 > 200)
+    assert f(ctypes.byref(c), 2, T, 64, 16, -1, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, T, 64, 16, 13, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
 
 
 def test_prefill_rejects_bad_arguments(lib):

@@ -603,3 +603,139 @@ def test_decode_on_slot_maps_from_the_page_pool():
     no_device_error()
     ref = oracle.decode(kb, vb, r2t, rpi, seq, q, 1, kv_indptr=kvi)
     assert_close(f64(o), ref, "bf16", "pool slot maps")
+
+
+def shared_case(batch, heads, ps, shared, priv_hi, seed, d=128, hk=8):
+    """A decode case whose rows share their first `shared` positions (whole
+    pages), each with 1 + U[0, priv_hi] private positions."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    kv = shared + rng.integers(0, priv_hi, size=batch, endpoint=True) + 1
+    pages = shared // ps + int(np.sum(-(-(kv - shared) // ps))) + 8
+    size = -(-pages * ps // 1024) * 1024
+    return W.make_case("shared", mode="decode", dtype="bf16", n_layers=2, layer_id=1, size=size,
+                       n_heads=heads, n_kv_heads=hk, head_dim=d, kv_lens=kv, page_size=ps,
+                       shared_prefix=shared, seed=seed, rng=rng)
+
+
+def test_prefix_shared_decode_reads_the_shared_pages_once_per_group():
+    """The prefix-shared workload with its 128 shared pages stated: equal to
+    the oracle, and (another summation order) not bit-identical to the decode
+    that reads every request's prefix."""
+    case = W.prefix_shared_decode()
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    table = torch.from_numpy(page_table(case)).cuda()
+    o = pkv.paged_decode_pages(cache, case.layer_id, table, case.page_size, q, workspace=ws,
+                               shared_pages=case.shared_prefix // case.page_size)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", "shared pages")
+    plain = pkv.paged_decode_pages(cache, case.layer_id, table, case.page_size, q, workspace=ws)
+    assert not torch.equal(o, plain)
+
+
+@pytest.mark.parametrize("batch,heads,ps,shared,priv_hi,d", [
+    (37, 8, 16, 512, 300, 128),      # G = 1: groups of 16 requests, the last one partial
+    (9, 16, 4, 256, 64, 128),        # G = 2: groups of 8, page_size 4
+    (5, 64, 32, 1024, 2000, 128),    # G = 8: pairs, long private tails
+    (3, 32, 1, 64, 10, 128),         # single-slot pages, the shortest shared prefix used
+    (40, 32, 16, 4096, 50, 128),     # long prefix: many group CTAs per group
+    (20, 32, 16, 1024, 200, 64),     # head_dim 64
+])
+def test_shared_prefix_variants(batch, heads, ps, shared, priv_hi, d):
+    case = shared_case(batch, heads, ps, shared, priv_hi, seed=batch * 7 + ps, d=d)
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    table = torch.from_numpy(page_table(case)).cuda()
+    o = pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, workspace=ws,
+                               shared_pages=shared // ps)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", f"shared {shared} ps={ps} G={heads // 8}")
+    plain = pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, workspace=ws)
+    assert not torch.equal(o, plain)   # the shared-prefix mode ran
+
+
+def test_shared_prefix_with_empty_private_parts_replays_in_a_cuda_graph():
+    """Entries whose context is exactly the shared prefix (no private
+    positions), captured once and replayed after the lengths change."""
+    case = shared_case(12, 32, 16, 768, 400, seed=41)
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    table = torch.from_numpy(page_table(case)).cuda()
+    lens = case.seq_lens.copy()
+    lens[[0, 5, 11]] = 768
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cache.seq_lens.copy_(torch.from_numpy(lens))
+    cache.kv_indptr.copy_(torch.from_numpy(indptr))
+    o = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    call = lambda: pkv.paged_decode_pages(cache, case.layer_id, table, 16, q, o, workspace=ws,
+                                          stream=s, shared_pages=48)
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    no_device_error()
+    ref = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                        lens, case.q, case.layer_id, kv_indptr=indptr)
+    assert_close(f64(o), ref, "bf16", "empty private parts")
+    eager = o.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, eager)
+    lens2 = case.seq_lens.copy()
+    lens2[[2, 3]] = 768
+    lens2[7] -= 1
+    indptr2 = np.concatenate([[0], np.cumsum(lens2)]).astype(np.int32)
+    cache.seq_lens.copy_(torch.from_numpy(lens2))
+    cache.kv_indptr.copy_(torch.from_numpy(indptr2))
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    ref2 = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         lens2, case.q, case.layer_id, kv_indptr=indptr2)
+    assert_close(f64(o), ref2, "bf16", "shared graph replay, new lengths")
+
+
+def test_false_shared_prefix_claims_are_reported_not_faulted():
+    """A row whose leading pages differ from its group's, or a context
+    shorter than the stated prefix: the device error word is set and the
+    call completes."""
+    case = shared_case(10, 32, 16, 512, 100, seed=77)
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    table = page_table(case)
+    bad = table.copy()
+    r = int(case.req_pool_indices[6])
+    bad[r, 3] = (bad[r, 3] + 1) % (case.k_buffer.shape[1] // 16)
+    pkv.paged_decode_pages(cache, case.layer_id, torch.from_numpy(bad).cuda(), 16, q, workspace=ws,
+                           shared_pages=32)
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX and detail == -3000 - 6
+    lens = case.seq_lens.copy()
+    lens[4] = 300   # below the 512 stated shared positions
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cache.seq_lens.copy_(torch.from_numpy(lens))
+    cache.kv_indptr.copy_(torch.from_numpy(indptr))
+    pkv.paged_decode_pages(cache, case.layer_id, torch.from_numpy(table).cuda(), 16, q,
+                           workspace=ws, shared_pages=32)
+    st, _ = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX
+
+
+@pytest.mark.parametrize("hk,shared_pages,splits", [(4, 32, 1024), (8, 3, 1024), (8, 32, 64)])
+def test_shared_prefix_statement_ignored_where_it_does_not_apply(hk, shared_pages, splits):
+    """4 kv heads, fewer than 64 shared positions, or a workspace without
+    room for the group partials: the decode runs as without the statement
+    (bit-identical)."""
+    case = shared_case(6, 4 * hk, 16, 512, 100, seed=88, hk=hk)
+    cache, q = prepare(case)
+    ws = ws_for(case, splits=splits)
+    table = torch.from_numpy(page_table(case)).cuda()
+    o = pkv.paged_decode_pages(cache, case.layer_id, table, 16, q, workspace=ws,
+                               shared_pages=shared_pages)
+    no_device_error()
+    assert torch.equal(o, pkv.paged_decode_pages(cache, case.layer_id, table, 16, q, workspace=ws))
