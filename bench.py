@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--decode-sweep", action="store_true",
                     help="print decode KV GB/s over batch x context (uniform contexts) and exit")
-    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "kvwrite"],
+    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "kvwrite", "prefix_shared"],
                     help="run a few untimed calls of one kernel's case (for ncu) and exit")
     return ap.parse_args()
 
@@ -108,7 +108,9 @@ def run_profile_case(which: str) -> None:
     """A few untimed calls of one workload, sized for an ncu capture (a few GB
     on the device at most): decode = the batched decode (98,304-slot pool),
     long = B=1 at 32,768 tokens, prefill = 4 ragged-prefill requests,
-    kvwrite = the ragged prefill's cache write (17,418 tokens)."""
+    kvwrite = the ragged prefill's cache write (17,418 tokens), prefix_shared =
+    the prefix-shared workload through the page table with its 128 shared
+    pages stated."""
     import torch
     import paged_kv_cache_loc_gb300 as pkv
     from paged_kv_cache_loc_gb300 import build
@@ -123,6 +125,17 @@ def run_profile_case(which: str) -> None:
         o = torch.empty_like(q)
         for _ in range(3):
             pkv.paged_decode(cache, case.layer_id, q, o, workspace=ws)
+    elif which == "prefix_shared":
+        case = W.prefix_shared_decode()
+        cache, q, kn, vn = W.upload(case)
+        pkv.kv_write(cache, case.layer_id, kn, vn)
+        ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1024)
+        o = torch.empty_like(q)
+        ps = case.page_size
+        table = torch.from_numpy(np.ascontiguousarray(case.req_to_token[:, ::ps] // ps)).cuda()
+        for _ in range(3):
+            pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, o, workspace=ws,
+                                   shared_pages=case.shared_prefix // ps)
     elif which == "prefill":
         case = W.ragged_prefill(batch=4, size=32768)
         cache, q, kn, vn = W.upload(case)
