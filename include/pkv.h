@@ -189,6 +189,24 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
                      int32_t n_heads, float sm_scale, const pkv_workspace *ws, void *stream);
 
 /*
+ * pkv_paged_decode with a shared prefix stated: the first shared_len
+ * positions of every request row of the batch (req_to_token[r, 0 ..
+ * shared_len), r = c->req_pool_indices[b]) hold the same slots, as when the
+ * prefix cache ("KVCache System") hands several tasks the same pages.  Same
+ * operation and result as pkv_paged_decode; with the balanced plan, 8 kv
+ * heads, shared_len >= 64, batch >= 2 and room in the workspace the shared
+ * rows are read once per group of 16 / G requests (see
+ * pkv_paged_decode_pages for the workspace it needs), otherwise the
+ * statement is ignored.  Every seq_len must be >= shared_len; a shorter
+ * context, or a row whose leading slots differ from its group's, is a
+ * device-data error.  shared_len < 0, or shared_len > c->max_len, returns
+ * PKV_ERR_ARG.
+ */
+int pkv_paged_decode_shared(const pkv_kvcache *c, int32_t layer_id, int32_t shared_len,
+                            const void *q, void *o, int32_t n_heads, float sm_scale,
+                            const pkv_workspace *ws, void *stream);
+
+/*
  * Paged decode through a page table ("KVCache System": the pool is made of
  * pages of page_size consecutive token slots; the 5-D view [n_layers,
  * n_pages, page_size, n_kv_heads, head_dim] is byte-identical to

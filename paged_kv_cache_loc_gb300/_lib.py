@@ -69,6 +69,9 @@ SIGNATURES = {
     "pkv_paged_decode": (ctypes.c_int, [ctypes.POINTER(PkvKVCache), ctypes.c_int32, _vp, _vp,
                                         ctypes.c_int32, ctypes.c_float,
                                         ctypes.POINTER(PkvWorkspace), _vp]),
+    "pkv_paged_decode_shared": (ctypes.c_int, [ctypes.POINTER(PkvKVCache), ctypes.c_int32,
+                                               ctypes.c_int32, _vp, _vp, ctypes.c_int32,
+                                               ctypes.c_float, ctypes.POINTER(PkvWorkspace), _vp]),
     "pkv_paged_decode_pages": (ctypes.c_int, [ctypes.POINTER(PkvKVCache), ctypes.c_int32, _vp,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
                                               ctypes.c_int32, ctypes.c_float,

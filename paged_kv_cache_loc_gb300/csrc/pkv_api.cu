@@ -334,6 +334,42 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
     return decode_impl(c, layer_id, q, o, n_heads, sm_scale, 0, ws, stream);
 }
 
+// Shared-prefix mode, when it applies and fits: the group role needs one
+// warp per kv head and at most 1024 group positions per CTA with at least
+// one CTA left for the private role; its partials follow the private rows in
+// the workspace.  Otherwise p is left as it is (the plain balanced decode).
+void use_shared_prefix(const pkv_kvcache *c, int32_t n_heads, int64_t shared_len,
+                       const pkv_workspace *ws, pkv::DecodeParams *p) {
+    const int group = n_heads / c->n_kv_heads;
+    if (shared_len < 64 || c->batch < 2 || c->n_kv_heads != 8 || !p->balanced ||
+        shared_len * c->batch > INT32_MAX)
+        return;
+    const int64_t reqs = 16 / group;
+    const int64_t n_groups = (c->batch + reqs - 1) / reqs;
+    const int64_t min_group_ctas = (n_groups * shared_len + 1023) / 1024;
+    const int64_t unit0 = (static_cast<int64_t>(p->n_parts) + c->batch) * n_heads;
+    const int64_t units = unit0 + (p->n_parts + n_groups) * reqs * n_heads;
+    if (p->n_parts < min_group_ctas + 1 || !ws_holds(ws, units, c->head_dim)) return;
+    p->shared_len = static_cast<int32_t>(shared_len);
+    p->group_reqs = static_cast<int32_t>(reqs);
+    p->n_groups = static_cast<int32_t>(n_groups);
+    p->group_unit0 = unit0;
+}
+
+int pkv_paged_decode_shared(const pkv_kvcache *c, int32_t layer_id, int32_t shared_len,
+                            const void *q, void *o, int32_t n_heads, float sm_scale,
+                            const pkv_workspace *ws, void *stream) {
+    if (!c) return PKV_ERR_ARG;
+    if (shared_len < 0 || (c->batch > 0 && shared_len > c->max_len)) return PKV_ERR_ARG;
+    pkv::DecodeParams p;
+    bool empty = false;
+    int rc = decode_prepare(c, layer_id, q, o, n_heads, sm_scale, 0, ws, &p, &empty);
+    if (rc || empty) return rc;
+    use_shared_prefix(c, n_heads, shared_len, ws, &p);
+    return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, n_heads / c->n_kv_heads,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t *req_to_page,
                            int32_t max_pages, int32_t page_size, int32_t shared_pages,
                            const void *q, void *o, int32_t n_heads, float sm_scale,
@@ -359,25 +395,7 @@ int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t
     p.max_pages = max_pages;
     p.page_size = page_size;
     p.n_pages = c->size / page_size;
-    // Shared-prefix mode, when it applies and fits: the group role needs one
-    // warp per kv head and at most 1024 group positions per CTA with at
-    // least one CTA left for the private role; its partials follow the
-    // private rows in the workspace.
-    const int group = n_heads / c->n_kv_heads;
-    if (shared_len >= 64 && c->batch >= 2 && c->n_kv_heads == 8 && p.balanced &&
-        shared_len * c->batch <= INT32_MAX) {
-        const int64_t reqs = 16 / group;
-        const int64_t n_groups = (c->batch + reqs - 1) / reqs;
-        const int64_t min_group_ctas = (n_groups * shared_len + 1023) / 1024;
-        const int64_t unit0 = (static_cast<int64_t>(p.n_parts) + c->batch) * n_heads;
-        const int64_t units = unit0 + (p.n_parts + n_groups) * reqs * n_heads;
-        if (p.n_parts >= min_group_ctas + 1 && ws_holds(ws, units, c->head_dim)) {
-            p.shared_len = static_cast<int32_t>(shared_len);
-            p.group_reqs = static_cast<int32_t>(reqs);
-            p.n_groups = static_cast<int32_t>(n_groups);
-            p.group_unit0 = unit0;
-        }
-    }
+    use_shared_prefix(c, n_heads, shared_len, ws, &p);
     return map_launch(pkv::launch_decode(p, c->dtype, c->head_dim, n_heads / c->n_kv_heads,
                                          static_cast<cudaStream_t>(stream)));
 }

@@ -148,6 +148,26 @@ def paged_decode(cache: KVCache, layer_id: int, q: torch.Tensor, o: Optional[tor
     return o
 
 
+def paged_decode_shared(cache: KVCache, layer_id: int, shared_len: int, q: torch.Tensor,
+                        o: Optional[torch.Tensor] = None, sm_scale: Optional[float] = None,
+                        workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """paged_decode with the statement that the first shared_len positions of
+    every request row in the batch hold the same slots; the decode may then
+    read those rows once per group of requests."""
+    c = cache.c_struct()
+    dev = cache.device
+    n_heads, head_dim = int(q.shape[1]), int(q.shape[2])
+    if o is None:
+        o = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(head_dim) if sm_scale is None else float(sm_scale)
+    rc = _lib.load().pkv_paged_decode_shared(ctypes.byref(c), layer_id, int(shared_len),
+                                             _need(q, "q", cache.k_buffer.dtype, dev),
+                                             _need(o, "o", cache.k_buffer.dtype, dev), n_heads,
+                                             scale, _ws(workspace), _stream(stream, dev))
+    check(rc, "pkv_paged_decode_shared")
+    return o
+
+
 def paged_decode_pages(cache: KVCache, layer_id: int, req_to_page: torch.Tensor, page_size: int,
                        q: torch.Tensor, o: Optional[torch.Tensor] = None,
                        sm_scale: Optional[float] = None, workspace: Optional[Workspace] = None,

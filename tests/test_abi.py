@@ -181,6 +181,15 @@ def test_paged_decode_pages_rejects_bad_arguments(lib):
     assert f(ctypes.byref(c), 2, T, 64, 16, 13, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
 
 
+def test_paged_decode_shared_rejects_bad_arguments(lib):
+    f = lib.pkv_paged_decode_shared
+    c = fake_cache()   # max_len 200
+    assert f(None, 2, 64, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, -1, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(c), 2, 201, Q, O, 32, 0.1, None, None) == _lib.PKV_ERR_ARG
+    assert f(ctypes.byref(fake_cache(batch=0)), 2, 64, Q, O, 32, 0.1, None, None) == _lib.PKV_OK
+
+
 def test_prefill_rejects_bad_arguments(lib):
     c = fake_cache(max_len=256)
 

@@ -739,3 +739,29 @@ def test_shared_prefix_statement_ignored_where_it_does_not_apply(hk, shared_page
                                shared_pages=shared_pages)
     no_device_error()
     assert torch.equal(o, pkv.paged_decode_pages(cache, case.layer_id, table, 16, q, workspace=ws))
+
+
+@pytest.mark.parametrize("heads,shared,batch", [(32, 2048, 64), (16, 320, 11)])
+def test_shared_prefix_through_req_to_token(heads, shared, batch):
+    """The per-token path with the shared prefix stated (slots compared at
+    every position): equal to the oracle, and not the plain decode's
+    summation order."""
+    case = shared_case(batch, heads, 16, shared, 500, seed=heads + shared)
+    cache, q = prepare(case)
+    ws = ws_for(case)
+    o = pkv.paged_decode_shared(cache, case.layer_id, shared, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), oracle_decode(case), "bf16", f"shared {shared} via req_to_token")
+    assert not torch.equal(o, pkv.paged_decode(cache, case.layer_id, q, workspace=ws))
+
+
+def test_shared_prefix_through_req_to_token_reports_a_differing_slot():
+    case = shared_case(8, 32, 1, 256, 40, seed=5)
+    cache, q = prepare(case)
+    r2t = case.req_to_token.copy()
+    r = int(case.req_pool_indices[5])
+    r2t[r, 100] = r2t[r, 101]   # one shared position of entry 5 points elsewhere
+    cache.req_to_token.copy_(torch.from_numpy(r2t))
+    pkv.paged_decode_shared(cache, case.layer_id, 256, q, workspace=ws_for(case))
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX and detail == -3000 - 5
