@@ -531,6 +531,7 @@ def run_pkv(args):
         out["prefill"] = prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev)
     if rank == 0 and not args.no_extras:
         out["cpu_baseline"] = cpu_baseline(case, b_dec + b_wr)
+        out["oracle_per_config"] = oracle_per_config(W)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -750,6 +751,57 @@ def cpu_baseline(case, step_bytes):
             "sample": "the full decode step (kv_write of 32 rows + decode of all 32 requests, "
                       "all heads), best of 2; pool restricted to the target layer "
                       f"(copy {t_copy:.2f}s, untimed)", "host_threads_available": os.cpu_count()}
+
+
+def oracle_per_config(W):
+    """The fp64 oracle (1 host core) on the other workloads, each on a bounded
+    sample: the B=1 32K decode whole, 8 of the 64 prefix-shared requests, and
+    ~4 sampled query rows per request of the ragged prefill (extrapolated to
+    the whole prefill by its count of unmasked (query, key) pairs)."""
+    import oracle
+    out = {}
+    case = W.long_decode(32768)
+    t0 = time.perf_counter()
+    oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                  case.seq_lens, case.q, case.layer_id)
+    t = time.perf_counter() - t0
+    out["b1_32k_decode"] = {"seconds": round(t, 3), "kv_gbs": round(decode_bytes(case) / t / 1e9, 4),
+                            "sample": "the whole decode"}
+    del case
+    case = W.prefix_shared_decode()
+    sel = np.arange(8)
+    t0 = time.perf_counter()
+    oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices[sel],
+                  case.seq_lens[sel], case.q[sel], case.layer_id)
+    t = time.perf_counter() - t0
+    row = case.n_kv_heads * case.head_dim * case.elem_bytes
+    logical = float(case.seq_lens[sel].sum()) * (2 * row + 4)
+    out["prefix_shared_decode"] = {"seconds": round(t, 3), "logical_kv_gbs": round(logical / t / 1e9, 4),
+                                   "sample": "8 of the 64 requests (all heads)",
+                                   "extrapolated_seconds": round(t * float(case.seq_lens.sum()) /
+                                                                 float(case.seq_lens[sel].sum()), 2)}
+    del case
+    case = W.ragged_prefill()
+    rows = W.prefill_sample_rows(case, n_random=1)
+    t0 = time.perf_counter()
+    oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                   case.qo_indptr, case.kv_indptr, case.q, case.layer_id, rows=rows)
+    t = time.perf_counter() - t0
+    # unmasked keys of each sampled row, against those of every row
+    seen = 0
+    for r in rows:
+        b = int(np.searchsorted(case.qo_indptr, r, side="right") - 1)
+        i = int(r - case.qo_indptr[b])
+        seen += int(case.kv_indptr[b + 1] - case.kv_indptr[b] - (case.qo_indptr[b + 1] - case.qo_indptr[b])) + i + 1
+    flops_sampled = 4.0 * case.head_dim * case.n_heads * seen
+    flops_all = prefill_flops(case)
+    out["ragged_prefill"] = {"seconds": round(t, 3), "rows": int(rows.size),
+                             "rows_per_s": round(rows.size / t, 2),
+                             "gflops": round(flops_sampled / t / 1e9, 3),
+                             "extrapolated_seconds": round(t * flops_all / flops_sampled, 1),
+                             "sample": f"{rows.size} query rows (per request rows 0, 1, q_len-1 and one "
+                                       "seeded row), all heads"}
+    return out
 
 
 # ---------------------------------------------------------------------------
