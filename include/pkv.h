@@ -20,7 +20,15 @@
  * replay sees stable addresses.
  *
  * Conventions for every entry point:
- *   - All tensors are caller-owned DEVICE memory, row-major and contiguous.
+ *   - All tensors are caller-owned, row-major and contiguous, in memory the
+ *     GPU can address: device or managed memory, or registered (pinned)
+ *     host memory mapped at the same address.  The pool, the index tables
+ *     and the workspace belong in device memory; a step's small inputs and
+ *     outputs (q, o, the new K/V rows, seq_lens, kv_indptr, qo_indptr,
+ *     req_pool_indices, out_cache_loc) may stay in pinned host memory, which
+ *     the kernels then read and write in place over the host link (on a
+ *     Grace-Blackwell node: NVLink-C2C).  Any other address (unregistered
+ *     host memory, say) returns PKV_ERR_ARG before anything is enqueued.
  *     The library never allocates, frees or copies host<->device.
  *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
  *     stream).  Work is enqueued asynchronously; the call returns once enqueued.

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "pkv.h"
@@ -47,6 +48,27 @@ int device_info(DeviceInfo *out) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Memory the kernels may dereference: device or managed memory, or
+// registered (pinned) host memory mapped at the same address, which the GPU
+// reads and writes over the host link.  Anything else (an unregistered host
+// address, say) is refused before launching, since touching it would fault
+// the device.  Null entries are optional arguments the caller checked.
+bool device_visible(const void *p) {
+    if (!p) return true;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // not sticky: clear it
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+int check_visible(std::initializer_list<const void *> ptrs) {
+    for (const void *p : ptrs)
+        if (!device_visible(p)) return PKV_ERR_ARG;
+    return PKV_OK;
+}
 
 int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
@@ -178,6 +200,9 @@ int decode_prepare(const pkv_kvcache *c, int32_t layer_id, const void *q, void *
     DeviceInfo di;
     rc = device_info(&di);
     if (rc) return rc;
+    rc = check_visible({c->k_buffer, c->v_buffer, c->req_to_token, c->req_pool_indices, c->seq_lens,
+                        c->kv_indptr, q, o, ws ? ws->base : nullptr});
+    if (rc) return rc;
     Plan plan;
     rc = make_plan(c, n_heads, di.sms, ws, chunk, &plan);
     if (rc) return rc;
@@ -253,6 +278,9 @@ int kv_write_prepare(const pkv_kvcache *c, int32_t layer_id, const void *k, cons
     }
     DeviceInfo di;
     rc = device_info(&di);
+    if (rc) return rc;
+    rc = check_visible({c->k_buffer, c->v_buffer, c->out_cache_loc, k, v, rope ? freqs_cis : nullptr,
+                        rope ? positions : nullptr});
     if (rc) return rc;
     pkv::KvWriteParams &p = *out;
     p = pkv::KvWriteParams{};
@@ -468,6 +496,9 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
     if (static_cast<int64_t>(max_q_len) * group / 64 + 1 > INT32_MAX) return PKV_ERR_ARG;
     DeviceInfo di;
     rc = device_info(&di);
+    if (rc) return rc;
+    rc = check_visible({c->k_buffer, c->v_buffer, c->req_to_token, c->req_pool_indices, c->qo_indptr,
+                        c->kv_indptr, q, o});
     if (rc) return rc;
     pkv::PrefillParams p{};
     p.q = q;

@@ -20,15 +20,20 @@ _DTYPES = {torch.float32: _lib.PKV_F32, torch.bfloat16: _lib.PKV_BF16}
 
 
 def _need(t: torch.Tensor, name: str, dtype=None, dev=None) -> int:
+    """The address of a CUDA tensor, or of a pinned host tensor (the kernels
+    then read or write it in place over the host link; the library checks
+    that it is mapped).  Unpinned host memory is refused: there is no CPU
+    path."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    host = not t.is_cuda
+    if host and not (t.device.type == "cpu" and torch.cuda.is_available() and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory (there is no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if dev is not None and t.device != dev:
+    if dev is not None and not host and t.device != dev:
         raise ValueError(f"{name} is on {t.device}, expected {dev}")
     return t.data_ptr()
 

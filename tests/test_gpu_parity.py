@@ -765,3 +765,85 @@ def test_shared_prefix_through_req_to_token_reports_a_differing_slot():
     pkv.paged_decode_shared(cache, case.layer_id, 256, q, workspace=ws_for(case))
     st, detail = pkv.last_device_error()
     assert st == _lib.PKV_ERR_INDEX and detail == -3000 - 5
+
+
+def _pinned(a):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if t.dtype == torch.int16:
+        t = t.view(torch.bfloat16)
+    return t.pin_memory()
+
+
+def _host_step_case():
+    case = W.batched_decode(batch=16, lo=200, hi=3000, size=65536, seed=919)
+    cache, q, kn, vn = W.upload(case)
+    host = {"q": _pinned(case.q.view(np.int16)), "k_new": _pinned(case.k_new.view(np.int16)),
+            "v_new": _pinned(case.v_new.view(np.int16)), "seq_lens": _pinned(case.seq_lens),
+            "req_pool_indices": _pinned(case.req_pool_indices),
+            "out_cache_loc": _pinned(case.out_cache_loc), "kv_indptr": _pinned(case.kv_indptr)}
+    hcache = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                         req_to_token=cache.req_to_token, req_pool_indices=host["req_pool_indices"],
+                         seq_lens=host["seq_lens"], out_cache_loc=host["out_cache_loc"],
+                         kv_indptr=host["kv_indptr"], max_len=case.max_len)
+    return case, cache, q, kn, vn, host, hcache
+
+
+def test_decode_step_reads_and_writes_pinned_host_memory():
+    """The step's inputs (q, the new rows, the metadata) and o in pinned host
+    memory: the kernels use them in place (no copies) and the result is
+    bit-identical to the step on device copies."""
+    case, cache, q, kn, vn, host, hcache = _host_step_case()
+    ws = ws_for(case, splits=64)
+    o_dev = pkv.decode_step(cache, case.layer_id, kn, vn, q, workspace=ws)
+    o_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    pkv.decode_step(hcache, case.layer_id, host["k_new"], host["v_new"], host["q"], o_host,
+                    workspace=ws)
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(o_host, o_dev.cpu())
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    check_pool_bit_exact(cache, case)
+
+
+def test_decode_step_graph_on_pinned_host_buffers():
+    """A serving loop without copies: the step captured once on pinned host
+    buffers; the host rewrites q in place between replays and reads o."""
+    case, cache, q, kn, vn, host, hcache = _host_step_case()
+    ws = ws_for(case, splits=64)
+    o_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    call = lambda: pkv.decode_step(hcache, case.layer_id, host["k_new"], host["v_new"], host["q"],
+                                   o_host, workspace=ws, stream=s)
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    rng = np.random.Generator(np.random.PCG64(3))
+    for _ in range(2):
+        bits = W._values(rng, case.q.shape, "bf16")
+        host["q"].copy_(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        no_device_error()
+        ref = pkv.decode_step(cache, case.layer_id, kn, vn, host["q"].cuda(), workspace=ws)
+        assert torch.equal(o_host, ref.cpu())
+
+
+def test_unregistered_host_memory_is_refused_before_launch():
+    """A plain (unpinned) host address would fault the device: the C ABI
+    refuses it with PKV_ERR_ARG and enqueues nothing."""
+    import ctypes
+    case = W.tiny_decode()
+    cache, q = prepare(case)
+    c = cache.c_struct()
+    plain = np.zeros(q.numel() * 2, np.uint8)   # q-sized, 16-byte aligned by numpy
+    assert plain.ctypes.data % 16 == 0
+    o = torch.empty_like(q)
+    rc = _lib.load().pkv_paged_decode(ctypes.byref(c), case.layer_id, ctypes.c_void_p(plain.ctypes.data),
+                                      ctypes.c_void_p(o.data_ptr()), case.n_heads, 0.125, None, None)
+    assert rc == _lib.PKV_ERR_ARG
+    no_device_error()
