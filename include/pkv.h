@@ -306,7 +306,7 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
  * while another component holds a stream capture open in global mode (where
  * cudaMalloc is not allowed), plugins inside engines whose allocator owns all
  * device memory, or latency-bound loops that cannot take cudaMalloc's
- * implicit synchronisation.  The paper has no counterpart: its decode always
+ * implicit synchronisation.  The pages have no counterpart: their decode always
  * receives a workspace.
  *
  * Same operation, arguments and results as pkv_paged_decode, but the split-K
