@@ -532,6 +532,7 @@ def run_pkv(args):
     if rank == 0 and not args.no_extras:
         out["cpu_baseline"] = cpu_baseline(case, b_dec + b_wr)
         out["oracle_per_config"] = oracle_per_config(W)
+        out["host_allocator"] = allocator_leg()
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -744,13 +745,31 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
     def attend():
         pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o,
                           stream=stream)
+    # the fused RoPE write of the same rows: standard rotary table
+    # (theta = 10000^(-2i/d), [max_pos, d/2, 2] f32), each new token at its
+    # position P + i in its request
+    d = case.head_dim
+    max_pos = int(case.seq_lens.max())
+    inv = 10000.0 ** (-np.arange(0, d, 2, dtype=np.float64) / d)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    table = torch.from_numpy(np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32)).to(dev)
+    pos = np.concatenate([np.arange(int(case.seq_lens[b] - case.q_lens[b]), int(case.seq_lens[b]))
+                          for b in range(case.batch)]).astype(np.int32)
+    positions = torch.from_numpy(pos).to(dev)
+
+    def rope_write():
+        pkv.rope_kv_write(cache, case.layer_id, kn, vn, table, positions, stream=stream)
     with torch.cuda.stream(stream):
+        ms_r, _ = timed(torch, stream, rope_write, args.prefill_steps, 3, flush)
+        # the plain write last, so the prefill attends to the unrotated rows
         ms, parts = timed(torch, stream, None, args.prefill_steps, 3, flush, parts=[write, attend])
     t_attn = statistics.mean(parts[1])
     t_wr = statistics.mean(parts[0])
+    t_rope = statistics.mean(ms_r)
     fl = prefill_flops(case)
     tf = fl / (t_attn * 1e-3) / 1e12
     wb = kv_write_bytes(case)
+    rb = wb + float(pos.size) * (4 + (d // 2) * 2 * 4)   # + position and table row per token
     return {"workload": "ragged causal prefill", "total_q": int(case.q_lens.sum()),
             "causal_flops": fl, "ms_prefill": round(t_attn, 4),
             "tflops": round(tf, 1), "roofline": {
@@ -759,7 +778,48 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
                 "peak_source": peaks["bf16_source"]},
             "kv_write_ms": round(t_wr, 4), "kv_write_gbs": round(wb / (t_wr * 1e-3) / 1e9, 1),
             "kv_write_frac_of_hbm": round(wb / (t_wr * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "rope_kv_write_ms": round(t_rope, 4),
+            "rope_kv_write_gbs": round(rb / (t_rope * 1e-3) / 1e9, 1),
+            "rope_kv_write_frac_of_hbm": round(rb / (t_rope * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "ms_per_step": round(statistics.mean(ms), 4)}
+
+
+def allocator_leg():
+    """The host page allocator (C++) on the prefix-shared workload's shapes:
+    64 tasks whose prompts share a 2048-token prefix (128 pages of 16) plus
+    U[0, 1024] private tokens, each allocated (prefix pages found by hash),
+    its hashes recorded, then all freed; 20 rounds.  The Python oracle of the
+    same allocator is timed on the same sequence."""
+    import oracle.pool_oracle as po
+    from paged_kv_cache_loc_gb300.pool import PagePool
+    rng = np.random.Generator(np.random.PCG64(1004))
+    prefix = rng.integers(0, 32000, 2048).tolist()
+    prompts = [prefix + rng.integers(0, 32000, int(n)).tolist()
+               for n in rng.integers(0, 1024, 64, endpoint=True)]
+    pages_per_round = sum(-(-len(p) // 16) for p in prompts)
+
+    def run(pool, record):
+        t0 = time.perf_counter()
+        for rnd in range(20):
+            for i, p in enumerate(prompts):
+                rc, _ = pool.task_alloc(rnd * 64 + i, p)
+                assert rc == 0
+                record(pool, rnd * 64 + i, p)
+            for i in range(64):
+                pool.task_free(rnd * 64 + i)
+        return time.perf_counter() - t0
+
+    t_py = run(po.PoolOracle(8192, 16), lambda pool, t, p: pool.task_record_hashes(t, p))
+    prompts = [np.asarray(p, np.int32) for p in prompts]   # the C++ pool takes int32 arrays
+    t_c = run(PagePool(8192, 16), lambda pool, t, p: pool.task_record_hashes(t, p))
+    n = 20 * 64
+    return {"tasks": n, "pages_mapped": 20 * pages_per_round,
+            "us_per_task": round(t_c / n * 1e6, 2),
+            "tasks_per_s": round(n / t_c, 1),
+            "oracle_us_per_task": round(t_py / n * 1e6, 2),
+            "what": "task_alloc (prefix lookup by page hash) + task_record_hashes + task_free, "
+                    "C++ pool through the ctypes binding on int32 prompt arrays; the Python "
+                    "oracle on the same sequence"}
 
 
 def cpu_baseline(case, step_bytes):
