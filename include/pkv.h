@@ -327,9 +327,17 @@ int pkv_paged_decode_noalloc(const pkv_kvcache *c, int32_t layer_id, const void 
 
 /*
  * Synchronise `stream`, then read and clear the calling device's error word.
- * Returns PKV_OK, PKV_ERR_INDEX (device data out of range since the last
- * read; *detail, if non-NULL, receives the first offending value) or
- * PKV_ERR_CUDA.
+ * Returns PKV_OK, PKV_ERR_INDEX (an error recorded on the device since the
+ * last read) or PKV_ERR_CUDA.  *detail, if non-NULL, receives the first
+ * recorded value: the offending slot, page, request row, length or position
+ * itself, or one of these codes:
+ *   -1000 - k      a decode wait on the copies of stage k gave up;
+ *   -2001, -2007   a prefill wait (producer, tensor-core thread) gave up;
+ *   -100000 - b    a shared prefix was stated, but entry b's leading pages (or
+ *                  slots) differ from those of its group's first entry;
+ *   -200000 - c    shared-prefix CTA c was handed more positions than it
+ *                  stages (not expected: the host sizes the grid for it).
+ * An offending value can itself be negative (a negative slot, say).
  */
 int pkv_last_device_error(void *stream, int64_t *detail);
 

@@ -854,7 +854,7 @@ __device__ __forceinline__ void stream_group(const DecodeParams &p, int cs, long
             const int len = static_cast<int>(min(t1, lo + Ts) - lo) - s0;
             if (len <= 0) continue;
             if (n == kMaxGroupPieces || off + ((len + 15) & ~15) > kDecodeMaxChunk) {
-                record_error(p.err, -4000 - cs);   // the host keeps ranges within these bounds
+                record_error(p.err, -200000 - cs);   // the host keeps ranges within these bounds
                 break;
             }
             int r = __ldg(p.req_pool_indices + gi * R);
@@ -954,7 +954,7 @@ __device__ __forceinline__ void stream_group(const DecodeParams &p, int cs, long
                 record_error(p.err, r);
                 continue;
             }
-            if (table_entry(p, r, jp) != lead) record_error(p.err, -3000 - b);
+            if (table_entry(p, r, jp) != lead) record_error(p.err, -100000 - b);
         }
     }
 

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             }
             if (!live && *s_abort == 0) {
                 *s_abort = 1;
-                record_error(p.err, -3001);
+                record_error(p.err, -2001);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && lane == 0 && *s_abort == 0) {
                 *s_abort = 1;
-                record_error(p.err, -3007);
+                record_error(p.err, -2007);
             }
             return ok;
         };

@@ -714,7 +714,7 @@ def test_false_shared_prefix_claims_are_reported_not_faulted():
     pkv.paged_decode_pages(cache, case.layer_id, torch.from_numpy(bad).cuda(), 16, q, workspace=ws,
                            shared_pages=32)
     st, detail = pkv.last_device_error()
-    assert st == _lib.PKV_ERR_INDEX and detail == -3000 - 6
+    assert st == _lib.PKV_ERR_INDEX and detail == -100000 - 6
     lens = case.seq_lens.copy()
     lens[4] = 300   # below the 512 stated shared positions
     indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -764,7 +764,7 @@ def test_shared_prefix_through_req_to_token_reports_a_differing_slot():
     cache.req_to_token.copy_(torch.from_numpy(r2t))
     pkv.paged_decode_shared(cache, case.layer_id, 256, q, workspace=ws_for(case))
     st, detail = pkv.last_device_error()
-    assert st == _lib.PKV_ERR_INDEX and detail == -3000 - 5
+    assert st == _lib.PKV_ERR_INDEX and detail == -100000 - 5
 
 
 def _pinned(a):
