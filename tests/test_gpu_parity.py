@@ -847,3 +847,32 @@ def test_unregistered_host_memory_is_refused_before_launch():
                                       ctypes.c_void_p(o.data_ptr()), case.n_heads, 0.125, None, None)
     assert rc == _lib.PKV_ERR_ARG
     no_device_error()
+
+
+def test_rope_kv_write_full_size():
+    """The fused RoPE write at the size the bench times it: the ragged
+    prefill's 17,418 new tokens, the standard rotary table, each token at its
+    position.  K within one bf16 rounding of the fp64 rotation, V and every
+    other pool row bit-exact."""
+    case = W.ragged_prefill()
+    d = case.head_dim
+    max_pos = int(case.seq_lens.max())
+    inv = 10000.0 ** (-np.arange(0, d, 2, dtype=np.float64) / d)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    fc = np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32)
+    pos = np.concatenate([np.arange(int(case.seq_lens[b] - case.q_lens[b]), int(case.seq_lens[b]))
+                          for b in range(case.batch)]).astype(np.int32)
+    cache, q, kn, vn = W.upload(case)
+    pkv.rope_kv_write(cache, case.layer_id, kn, vn, torch.from_numpy(fc).cuda(), torch.from_numpy(pos).cuda())
+    no_device_error()
+    k_rot = oracle.rope(case.k_new, fc, pos)
+    got_k = f64(cache.k_buffer)[case.layer_id, case.out_cache_loc]
+    assert np.all(np.abs(got_k - k_rot) <= np.abs(k_rot) * 2.0 ** -8 + 1e-6)
+    vb = W.host_of(cache.v_buffer)
+    assert np.array_equal(vb[case.layer_id, case.out_cache_loc], case.v_new)
+    # rows the write does not touch keep their contents
+    kb = W.host_of(cache.k_buffer)
+    mask = np.ones(case.k_buffer.shape[1], bool)
+    mask[case.out_cache_loc] = False
+    assert np.array_equal(kb[case.layer_id][mask], case.k_buffer[case.layer_id][mask])
+    assert np.array_equal(vb[case.layer_id][mask], case.v_buffer[case.layer_id][mask])
