@@ -23,6 +23,14 @@
 //    them through one ring (stream_pieces); otherwise piece by piece.
 // Slots come from req_to_token, or from a page table (slot_at).  The merge of
 // the balanced partition (decode_merge_balanced_kernel) is at the end.
+//
+// Shared prefix (the caller states that the first shared_len positions of
+// every row hold the same slots, as when prefix-cache hits give several
+// requests the same pages): a separate instantiation of the all-heads kernel
+// splits its CTAs into a group role (stream_group: the prefix read once per
+// group of 16 / G requests, whose heads are the 16 columns of two n8 tiles,
+// block_math2) and a private role (the balanced pass over the positions
+// past the prefix); decode_merge_shared_kernel merges both kinds of pieces.
 #include <atomic>
 
 #include "pkv_common.cuh"
