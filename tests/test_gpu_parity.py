@@ -876,3 +876,23 @@ def test_rope_kv_write_full_size():
     mask[case.out_cache_loc] = False
     assert np.array_equal(kb[case.layer_id][mask], case.k_buffer[case.layer_id][mask])
     assert np.array_equal(vb[case.layer_id][mask], case.v_buffer[case.layer_id][mask])
+
+
+def test_kv_write_and_prefill_on_pinned_host_memory():
+    """The cache write from new rows and locations in pinned host memory, and
+    the prefill reading q from and writing o to pinned host memory: the same
+    bits as with device copies."""
+    case = W.ragged_prefill(batch=3, q_hi=300, p_hi=500, size=8192, seed=77)
+    cache_d, q, kn, vn = W.upload(case)
+    pkv.kv_write(cache_d, case.layer_id, kn, vn)
+    o_d = pkv.paged_prefill(cache_d, case.layer_id, q, case.max_q_len, case.max_len)
+    cache_h, _, _, _ = W.upload(case)
+    cache_h.out_cache_loc = cache_h.out_cache_loc.cpu().pin_memory()
+    pkv.kv_write(cache_h, case.layer_id, kn.cpu().pin_memory(), vn.cpu().pin_memory())
+    torch.cuda.synchronize()
+    assert torch.equal(cache_h.k_buffer, cache_d.k_buffer) and torch.equal(cache_h.v_buffer, cache_d.v_buffer)
+    o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    pkv.paged_prefill(cache_h, case.layer_id, q.cpu().pin_memory(), case.max_q_len, case.max_len, o=o_h)
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(o_h, o_d.cpu())
