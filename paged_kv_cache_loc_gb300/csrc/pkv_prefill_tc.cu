@@ -212,10 +212,15 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     const int qo0 = __ldg(p.qo_indptr + b);
     const int q_len = __ldg(p.qo_indptr + b + 1) - qo0;
     const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-    if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 ||
+    // q and o hold qo_indptr[batch] packed rows: this entry's rows must lie
+    // inside them, or they are neither read nor written
+    const long long q_total = __ldg(p.qo_indptr + p.batch);
+    const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
+    if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
         q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
         if (qp == 0 && g == 0 && tid == 0)
-            record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r : kv_len);
+            record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
+                                : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
         return;
     }
     const int rows = q_len * G;

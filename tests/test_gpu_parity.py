@@ -165,7 +165,7 @@ def test_ragged_prefill_full_size_sampled():
     case = W.ragged_prefill()
     cache, q, o = run_prefill(case)
     check_pool_bit_exact(cache, case)
-    rows = W.prefill_sample_rows(case, n_random=16)
+    rows = W.prefill_sample_rows(case, n_random=64)
     ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
                          case.qo_indptr, case.kv_indptr, case.q, case.layer_id, rows=rows)
     assert_close(f64(o)[rows], ref, "bf16", "full prefill (sampled rows)")
@@ -302,6 +302,37 @@ def test_device_data_errors_are_reported_not_faulted(hk, indptr):
     o = pkv.paged_decode(cache, 1, q, workspace=ws)
     no_device_error()
     assert_close(f64(o), oracle_decode(case), "bf16", "after errors")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_prefill_rows_outside_q_are_reported_not_touched(d):
+    """A qo_indptr entry whose packed rows fall outside [0, qo_indptr[batch])
+    is recorded and its rows are neither read nor written.  q and o are
+    views into buffers padded by 64 rows on each side, so that even an
+    unchecked access would stay inside the allocation."""
+    case = W.make_case("bad_qo", mode="prefill", dtype="bf16", n_layers=2, layer_id=1, size=1024,
+                       n_heads=8, n_kv_heads=4, head_dim=d, kv_lens=[30, 50], q_lens=[20, 40],
+                       seed=21)
+    cache, q = prepare(case)
+    pad = 64
+    qp = torch.zeros(pad + q.shape[0] + pad, *q.shape[1:], dtype=q.dtype, device="cuda")
+    qp[pad:pad + q.shape[0]] = q
+    op = torch.full_like(qp, 7.0)
+    for qo in ([-20, 0, 40], [0, 30, 20]):
+        # entry 0 starts before row 0, or entry 1 ends past qo_indptr[batch]
+        bad = pkv.KVCache(k_buffer=cache.k_buffer, v_buffer=cache.v_buffer,
+                          req_to_token=cache.req_to_token, req_pool_indices=cache.req_pool_indices,
+                          kv_indptr=cache.kv_indptr, max_len=case.max_len,
+                          qo_indptr=torch.tensor(qo, dtype=torch.int32, device="cuda"))
+        pkv.paged_prefill(bad, case.layer_id, qp[pad:pad + q.shape[0]], 40, case.max_len,
+                          o=op[pad:pad + q.shape[0]])
+        assert pkv.last_device_error()[0] == _lib.PKV_ERR_INDEX
+        assert torch.all(op[:pad] == 7.0) and torch.all(op[-pad:] == 7.0), "padding was written"
+    # the context is still healthy and the word was cleared
+    _, _, o = run_prefill(case)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id)
+    assert_close(f64(o), ref, "bf16", "prefill after errors")
 
 
 def _short_lens(kind):
