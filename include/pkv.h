@@ -41,6 +41,11 @@
  *     error word and finishes; pkv_last_device_error() reports it.  Results
  *     of a call that recorded such an error are unspecified.
  *   - Nothing traps, aborts or waits without a bound.
+ *   - The library looks up the device addresses of its own device-resident
+ *     objects (the error word, the array of pkv_paged_decode_noalloc) once
+ *     per device and keeps them for the life of the process.  After
+ *     cudaDeviceReset() on a device those addresses are stale: make no
+ *     further pkv_* call on that device in the same process.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -316,9 +321,11 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
  * partials live in a library-owned device array of 8 MiB (a file-scope
  * __device__ object that every GPU loading the library holds until the
  * process exits).  Nothing is allocated or freed.  The number of splits is
- * capped by what fits in the array for batch x n_heads x head_dim; a call
- * that cannot fit even one split per (entry, head), or whose contexts would
- * then need chunks over 2048 tokens, returns PKV_ERR_WORKSPACE.
+ * capped by what fits in the array for batch x n_heads x head_dim.  When not
+ * even one split per (entry, head) fits, contexts of up to 2048 tokens
+ * (c->max_len <= 2048) are decoded in one split with o written directly;
+ * longer ones, or contexts that would need chunks over 2048 tokens, return
+ * PKV_ERR_WORKSPACE.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call on a device shares the one array

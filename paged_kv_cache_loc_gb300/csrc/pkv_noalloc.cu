@@ -57,7 +57,13 @@ int pkv_paged_decode_noalloc(const pkv_kvcache *c, int32_t layer_id, const void 
         if (need == 0 || need > kStaticScratchBytes) break;
         splits = s;
     }
-    if (splits == 0) return PKV_ERR_WORKSPACE;   // batch * n_heads too large for the array
+    if (splits == 0) {
+        // Not even one split per (entry, head) fits.  Contexts that one split
+        // covers need no partials: the decode writes o directly.
+        if (c->max_len <= pkv::kDecodeMaxChunk)
+            return pkv_paged_decode(c, layer_id, q, o, n_heads, sm_scale, nullptr, stream);
+        return PKV_ERR_WORKSPACE;
+    }
     void *base = nullptr;
     int rc = scratch_address(&base);
     if (rc) return rc;
