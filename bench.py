@@ -414,6 +414,12 @@ def timed(torch, stream, fn, steps, warmup, flush, parts=None):
     return total, (per_part if parts else None)
 
 
+def tstats(ms):
+    """Mean and median of per-rep times (ms) in microseconds, with the rep count."""
+    return {"mean_us": round(statistics.mean(ms) * 1e3, 2),
+            "median_us": round(statistics.median(ms) * 1e3, 2), "reps": len(ms)}
+
+
 def run_pkv(args):
     import torch
     import paged_kv_cache_loc_gb300 as pkv
@@ -517,6 +523,9 @@ def run_pkv(args):
         "step_call": ("pkv_decode_step (kv_write, then the decode split kernel as its programmatic "
                       "dependent, then the merge)" if chunk == 0 else "pkv_kv_write + pkv_paged_decode_chunked"),
         "decode_only_ms": round(ms_decode, 5),
+        "timing": {"statistic": "mean of the timed reps (value, ms_per_step); medians beside",
+                   "step": tstats(step_ms), "kv_write": tstats(parts[0]),
+                   "decode": tstats(parts[1])},
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -548,7 +557,8 @@ def graph_step_leg(torch, step, stream, flush, args, step_bytes, eager_ms, peaks
         ms, g = graph_replay_ms(torch, stream, step.fused, args.steps, args.warmup, flush)
     t = statistics.mean(ms)
     del g
-    return {"us_per_step": round(t * 1e3, 2), "kv_gbs": round(step_bytes / (t * 1e-3) / 1e9, 1),
+    return {"us_per_step": round(t * 1e3, 2), "timing": tstats(ms),
+            "kv_gbs": round(step_bytes / (t * 1e-3) / 1e9, 1),
             "frac_of_hbm_peak": round(step_bytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "eager_us_per_step": round(eager_ms * 1e3, 2),
             "what": "pkv_decode_step captured in a CUDA graph, replayed; L2 flushed before each replay"}
@@ -608,6 +618,7 @@ def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     b = decode_bytes(case) + kv_write_bytes(case)
     t = statistics.mean(ms)
     copies = {"value": round(b / (t * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(t, 5),
+              "timing": tstats(ms),
               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
               "path": ("one pinned host -> device copy of the packed step inputs (q, k_new, v_new, "
                        "seq_lens, req_pool_indices, out_cache_loc, kv_indptr), the public API call, "
@@ -640,6 +651,7 @@ def e2e_leg(torch, pkv, lib, case, cache, ws, chunk, stream, flush, args, dev):
     assert torch.equal(ho2, ho)
     t2 = statistics.mean(ms2)
     return {"value": round(b / (t2 * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(t2, 5),
+            "timing": tstats(ms2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "path": ("the public API call (decode_step) on pinned host buffers: the kernels read q, "
                      "k_new, v_new and the metadata (seq_lens, req_pool_indices, out_cache_loc, "
@@ -672,7 +684,8 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
         tg = statistics.mean(gms)
         b = decode_bytes(case)
         gbs = b / (t * 1e-3) / 1e9
-        sweep.append({"context": ctx, "us_per_decode": round(t * 1e3, 2), "kv_gbs": round(gbs, 1),
+        sweep.append({"context": ctx, "us_per_decode": round(t * 1e3, 2), "timing": tstats(ms),
+                      "graph_timing": tstats(gms), "kv_gbs": round(gbs, 1),
                       "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
                       "graph_us_per_decode": round(tg * 1e3, 2),
                       "graph_frac_of_hbm_peak": round(b / (tg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -682,7 +695,7 @@ def long_context_leg(torch, pkv, W, stream, flush, peaks, dev):
         del cache, q, kn, vn, ws, o
     out = dict(sweep[-1])
     out["sweep"] = [{k: s[k] for k in ("context", "us_per_decode", "kv_gbs", "frac_of_hbm_peak",
-                                       "graph_us_per_decode")}
+                                       "graph_us_per_decode", "timing")}
                     for s in sweep]
     return out
 
@@ -715,18 +728,19 @@ def prefix_shared_leg(torch, pkv, W, stream, flush, peaks, dev):
            "call": f"paged_decode_pages with shared_pages={n_shared} (the shared pages are read once "
                    f"per group of 16 / G requests)"}
 
-    def rates(t):
-        return {"us_per_decode": round(t * 1e3, 2),
+    def rates(ms):
+        t = statistics.mean(ms)
+        return {"us_per_decode": round(t * 1e3, 2), "timing": tstats(ms),
                 "logical_gbs": round(logical / (t * 1e-3) / 1e9, 1),
                 "unique_gbs": round(unique / (t * 1e-3) / 1e9, 1),
                 "unique_frac_of_hbm_peak": round(unique / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
     with torch.cuda.stream(stream):
         for name, fl in (("l2_flushed", flush), ("l2_warm", lambda: None)):
             ms, _ = timed(torch, stream, call, 100, 10, fl)
-            out[name] = rates(statistics.mean(ms))
+            out[name] = rates(ms)
         # the same decode without the statement: every request reads the prefix
         ms, _ = timed(torch, stream, plain, 100, 10, flush)
-        out["without_shared_pages_l2_flushed"] = rates(statistics.mean(ms))
+        out["without_shared_pages_l2_flushed"] = rates(ms)
     st, detail = pkv.last_device_error(stream, dev)
     if st != 0:
         raise RuntimeError(f"device error word set in the prefix-shared leg (detail {detail})")
@@ -781,7 +795,9 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
             "rope_kv_write_ms": round(t_rope, 4),
             "rope_kv_write_gbs": round(rb / (t_rope * 1e-3) / 1e9, 1),
             "rope_kv_write_frac_of_hbm": round(rb / (t_rope * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "ms_per_step": round(statistics.mean(ms), 4)}
+            "ms_per_step": round(statistics.mean(ms), 4),
+            "timing": {"prefill": tstats(parts[1]), "kv_write": tstats(parts[0]),
+                       "rope_kv_write": tstats(ms_r)}}
 
 
 def allocator_leg():
