@@ -726,7 +726,8 @@ def prefix_shared_leg(torch, pkv, W, stream, flush, peaks, dev):
     out = {"batch": case.batch, "page_size": ps, "shared_prefix_tokens": case.shared_prefix,
            "logical_bytes": logical, "unique_bytes": unique,
            "call": f"paged_decode_pages with shared_pages={n_shared} (the shared pages are read once "
-                   f"per group of 16 / G requests)"}
+                   f"per launch by a tensor-core kernel over all requests' query heads; the private "
+                   f"pages by the split kernel on the other SMs)"}
 
     def rates(ms):
         t = statistics.mean(ms)

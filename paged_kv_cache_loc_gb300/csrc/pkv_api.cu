@@ -362,16 +362,54 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
     return decode_impl(c, layer_id, q, o, n_heads, sm_scale, 0, ws, stream);
 }
 
-// Shared-prefix mode, when it applies and fits: the group role needs one
-// warp per kv head and at most 1024 group positions per CTA with at least
-// one CTA left for the private role; its partials follow the private rows in
-// the workspace.  Otherwise p is left as it is (the plain balanced decode).
+// Shared-prefix mode, when it applies and fits; otherwise p is left as it is
+// (the plain balanced decode).  Its partials follow the private rows in the
+// workspace.
+//  - head_dim 128: the prefix is read once per launch, by a tensor-core
+//    kernel over all batch x G query rows of each kv head (256 rows per CTA),
+//    the prefix cut into chunks of at most kGroupChunk positions; the private
+//    role takes the SMs that kernel leaves free.
+//  - head_dim 64: the group role runs inside the split kernel, one warp per
+//    kv head, at most 1024 group positions per CTA, with at least one CTA
+//    left for the private role; the prefix is read once per group of 16 / G
+//    requests.
+// Prefix positions per group-role CTA: four 128-key tiles.  On the
+// prefix-shared workload (64 requests, 2048 shared positions, 8 kv heads) that
+// is 32 group CTAs, which end before the private role on the other 120 SMs.
+constexpr int64_t kGroupChunk = 512;
+
 void use_shared_prefix(const pkv_kvcache *c, int32_t n_heads, int64_t shared_len,
                        const pkv_workspace *ws, pkv::DecodeParams *p) {
     const int group = n_heads / c->n_kv_heads;
     if (shared_len < 64 || c->batch < 2 || c->n_kv_heads != 8 || !p->balanced ||
         shared_len * c->batch > INT32_MAX)
         return;
+    if (c->head_dim == 128) {
+        DeviceInfo di;
+        if (device_info(&di) != PKV_OK) return;
+        const int64_t row_blocks = (static_cast<int64_t>(c->batch) * group + pkv::kGroupRows - 1) /
+                                   pkv::kGroupRows;
+        int64_t chunks = (shared_len + kGroupChunk - 1) / kGroupChunk;
+        const int64_t chunk_len = ((shared_len + chunks - 1) / chunks + 127) / 128 * 128;
+        chunks = (shared_len + chunk_len - 1) / chunk_len;
+        const int64_t group_ctas = chunks * c->n_kv_heads * row_blocks;
+        int64_t parts = di.sms - group_ctas;
+        if (parts > p->n_parts) parts = p->n_parts;
+        if (parts < 1) parts = 1;
+        const int64_t unit0 = (parts + c->batch) * n_heads;
+        if (row_blocks > 65535 || !ws_holds(ws, unit0 + chunks * c->batch * n_heads, c->head_dim))
+            return;
+        p->n_parts = static_cast<int32_t>(parts);
+        p->n_splits = static_cast<int32_t>(parts);
+        p->shared_len = static_cast<int32_t>(shared_len);
+        p->group_tc = 1;
+        p->group_chunks = static_cast<int32_t>(chunks);
+        p->group_chunk_len = static_cast<int32_t>(chunk_len);
+        p->group_reqs = 1;
+        p->n_groups = static_cast<int32_t>(c->batch);
+        p->group_unit0 = unit0;
+        return;
+    }
     const int64_t reqs = 16 / group;
     const int64_t n_groups = (c->batch + reqs - 1) / reqs;
     const int64_t min_group_ctas = (n_groups * shared_len + 1023) / 1024;

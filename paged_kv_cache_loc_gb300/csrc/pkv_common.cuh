@@ -43,6 +43,24 @@ __device__ __forceinline__ void cp_async_wait() {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// Partial stores with L2 evict_last priority: the merge reads the split-K
+// partials after a K/V stream that is usually larger than L2 and would
+// otherwise push the early ones out to DRAM.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_keep(float *addr, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(addr), "f"(v), "l"(pol) : "memory");
+}
+// 16-byte aligned float4 store with the same policy
+__device__ __forceinline__ void st_keep4(float *addr, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(addr), "f"(a),
+                 "f"(b), "f"(c), "f"(d), "l"(pol)
+                 : "memory");
+}
+
 template <typename T>
 struct Elem;
 template <>

@@ -111,17 +111,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
     return false;
 }
-// Partial stores with L2 evict_last priority: the merge reads the partials
-// right after the split, whose K/V stream (usually larger than L2) would
-// otherwise push the early ones out to DRAM.
-__device__ __forceinline__ uint64_t l2_keep_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void st_keep(float *addr, float v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(addr), "f"(v), "l"(pol) : "memory");
-}
 
 // Wait for the grid this one depends on programmatically (the cache write
 // of a decode step) to complete and its writes to become visible.
@@ -489,7 +478,11 @@ __device__ __forceinline__ SharedRoles shared_roles(const DecodeParams &p, long 
     r.t_sh = static_cast<long long>(p.n_groups) * p.shared_len;
     r.t_pr = T - static_cast<long long>(p.batch) * p.shared_len;
     const int P = p.n_parts;
-    if (r.t_pr <= 0) {
+    if (p.group_tc) {   // the group role is a kernel of its own
+        r.t_sh = 0;
+        r.p_sh = 0;
+        r.p_pr = P;
+    } else if (r.t_pr <= 0) {
         r.p_sh = P;
         r.p_pr = 0;
     } else {
@@ -1547,8 +1540,12 @@ __global__ void __launch_bounds__(256, 4) decode_merge_shared_kernel(const Decod
                 np_pr = part_of(phi - 1, ro.t_pr, ro.p_pr_e) - c_lo + 1;
             }
         }
-        cs_lo = part_of(gi * Ts, ro.t_sh, ro.p_sh_e);
-        np_sh = part_of((gi + 1) * Ts - 1, ro.t_sh, ro.p_sh_e) - cs_lo + 1;
+        if (p.group_tc) {   // one partial per chunk of the prefix
+            np_sh = p.group_chunks;
+        } else {
+            cs_lo = part_of(gi * Ts, ro.t_sh, ro.p_sh_e);
+            np_sh = part_of((gi + 1) * Ts - 1, ro.t_sh, ro.p_sh_e) - cs_lo + 1;
+        }
     }
     // the partials come from the split kernel, which may still run (the
     // piece lists above need only the metadata)
@@ -1573,8 +1570,10 @@ __global__ void __launch_bounds__(256, 4) decode_merge_shared_kernel(const Decod
             if (i < np) {
                 const int64_t unit =
                     i < np_pr ? (static_cast<int64_t>(c_lo) + i + b) * p.n_heads + h
-                              : p.group_unit0 +
-                                    ((static_cast<int64_t>(cs_lo) + (i - np_pr) + gi) * R + u) * p.n_heads + h;
+                    : p.group_tc
+                        ? p.group_unit0 + (static_cast<int64_t>(i - np_pr) * p.batch + b) * p.n_heads + h
+                        : p.group_unit0 +
+                              ((static_cast<int64_t>(cs_lo) + (i - np_pr) + gi) * R + u) * p.n_heads + h;
                 const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ml_part) + unit);
                 m[k] = ml.x;
                 l[k] = ml.y;
@@ -1704,6 +1703,12 @@ cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cu
 
 cudaError_t launch_decode_split_mma(const DecodeParams &p, int head_dim, int group,
                                     cudaStream_t s) {
+    if (p.group_tc) {   // the private role, then the shared prefix on tensor cores as its dependent
+        if (head_dim != 128) return cudaErrorNotSupported;
+        const cudaError_t e = run_group<128>(p, group, s);
+        if (e != cudaSuccess) return e;
+        return launch_shared_group_tc(p, group, s);
+    }
     return head_dim == 128 ? run_group<128>(p, group, s) : run_group<64>(p, group, s);
 }
 

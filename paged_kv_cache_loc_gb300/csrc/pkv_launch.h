@@ -82,6 +82,19 @@ struct DecodeParams {
     int32_t group_reqs;
     int32_t n_groups;
     int64_t group_unit0;
+    // Shared prefix read once per launch (bf16, head_dim 128): the group role
+    // is a separate tensor-core kernel (launch_shared_group_tc) over all
+    // batch x G query rows of each kv head, one CTA per (prefix chunk of
+    // group_chunk_len positions, kv head, 256 query rows); its partial of
+    // chunk k for entry b, head h is unit group_unit0 + (k * batch + b) *
+    // n_heads + h.  All n_parts CTAs of the split kernel take the private
+    // role.  The group kernel is launched as a programmatic dependent of the
+    // split kernel, on the SMs the split leaves free, and waits for it
+    // (griddepcontrol.wait) only before it exits; the merge, launched as the
+    // group kernel's dependent, then sees both.
+    int32_t group_tc;
+    int32_t group_chunks;
+    int32_t group_chunk_len;
 };
 
 // Ragged causal prefill.
@@ -106,6 +119,22 @@ struct PrefillParams {
     int32_t max_kv_len;
     float scale_log2;
     DevErr *err;
+    // Shared-prefix group role (launch_shared_group_tc), not used by the
+    // prefill: rows are the batch x G (entry, head) pairs of q [batch,
+    // n_heads, head_dim]; the keys are positions [0, shared_len) of the
+    // first entry's row (req_to_token, or the page table when page_size >
+    // 0), chunk_len of them per CTA; each CTA writes fp32 partials (o / l,
+    // then (m, l)) for its rows to o_part / ml_part at unit0 + (chunk *
+    // batch + b) * n_heads + h.
+    const int32_t *req_to_page;
+    int32_t max_pages;
+    int32_t page_size;
+    int64_t n_pages;
+    int32_t shared_len;
+    int32_t chunk_len;
+    float *o_part;
+    float *ml_part;
+    int64_t unit0;
 };
 
 constexpr int kDecodeMaxChunk = 2048;   // slot indices staged per split (or per piece)
@@ -133,5 +162,9 @@ bool prefill_supported(int dtype, int head_dim, int group);
 // tcgen05 (TMEM) prefill for bf16 head_dim 128 (pkv_prefill_tc.cu).
 bool prefill_tc_supported(int dtype, int head_dim, int group);
 cudaError_t launch_prefill_tc(const PrefillParams &p, int group, cudaStream_t s);
+// The shared-prefix group role of a decode with p.group_tc set
+// (pkv_prefill_tc.cu); launched before the split kernel.
+cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_t s);
+constexpr int kGroupRows = 256;          // query rows per group-role CTA (two 128-row tiles)
 
 }  // namespace pkv

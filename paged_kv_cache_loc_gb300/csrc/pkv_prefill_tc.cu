@@ -75,6 +75,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.f;                            // lazy rescale threshold (log2 units)
 static_assert(kSmemAbort + 4 <= kSmemRed, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kGroupRows == 2 * kRows, "a group-role CTA holds two query tiles");
+// group-role epilogue: each softmax warp stages 32 rows x 64 fp32 columns with
+// a 16-byte row pad (conflict-free 16-byte stores) in the query + K tile area
+constexpr int kStgPitch = 68;
+static_assert(kSoftmaxWarps * 32 * kStgPitch * 4 <= kSmemV - kSmemQ, "epilogue staging fits the Q and K tiles");
 
 // byte offset of 16-byte chunk `ch` (0..15) of row r
 __device__ __forceinline__ uint32_t sw_chunk(int r, int ch) {
@@ -193,7 +198,14 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
 }
-template <int G>
+// kGroup = false: the ragged prefill, one CTA per (query-tile pair, kv head,
+// entry).  kGroup = true: the group role of a shared-prefix decode, one CTA
+// per (chunk of the shared prefix, kv head, 256 query rows): the rows are the
+// (entry b, head-in-group) pairs of the decode's q [batch, n_heads, D], the
+// keys are the chunk's positions of the first entry's request row, nothing is
+// masked, and the CTA ends with fp32 partials (o / l and (m, l)) that the
+// decode's merge folds in.  Both share the pipeline below.
+template <int G, bool kGroup>
 __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams p) {
     using bf16 = __nv_bfloat16;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -204,48 +216,94 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     float *s_red = reinterpret_cast<float *>(sm + kSmemRed);
     auto bar = [&](int i) -> uint32_t { return s_base + kSmemBar + 8 * i; };
 
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int qp = gridDim.x - 1 - blockIdx.x;   // longest causal work first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    int r = __ldg(p.req_pool_indices + b);
-    const int qo0 = __ldg(p.qo_indptr + b);
-    const int q_len = __ldg(p.qo_indptr + b + 1) - qo0;
-    const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-    // q and o hold qo_indptr[batch] packed rows: this entry's rows must lie
-    // inside them, or they are neither read nor written
-    const long long q_total = __ldg(p.qo_indptr + p.batch);
-    const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
-    if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
-        q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
-        if (qp == 0 && g == 0 && tid == 0)
-            record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
-                                : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
-        return;
-    }
-    const int rows = q_len * G;
-    const int row0 = qp * 2 * kRows;
-    if (row0 >= rows) return;
-    const int P = kv_len - q_len;
-    // K/V tiles each query tile sees (0: the tile has no rows); B sees at least as many as A
+    const int g = blockIdx.y;
+    int qp, r, qo0, rows, kv_lo = 0, chunk = 0;
     int n_x[2], kv_end = 0;
+    int lim_pos = 0;   // group: last key position of the chunk
+    int P = 0;
+    if constexpr (kGroup) {
+        // the merge may launch now; it waits for this grid before reading
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+        chunk = blockIdx.x;
+        qp = blockIdx.z;
+        r = __ldg(p.req_pool_indices);   // the shared prefix is read from the first entry's row
+        if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs)) {
+            if (chunk == 0 && g == 0 && qp == 0 && tid == 0) record_error(p.err, r);
+            r = 0;
+        }
+        qo0 = 0;
+        rows = p.batch * G;
+        kv_lo = chunk * p.chunk_len;
+        kv_end = min(p.shared_len, kv_lo + p.chunk_len);
+        lim_pos = kv_end - 1;
+    } else {
+        const int b = blockIdx.z;
+        qp = gridDim.x - 1 - blockIdx.x;   // longest causal work first
+        r = __ldg(p.req_pool_indices + b);
+        qo0 = __ldg(p.qo_indptr + b);
+        const int q_len = __ldg(p.qo_indptr + b + 1) - qo0;
+        const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+        // q and o hold qo_indptr[batch] packed rows: this entry's rows must lie
+        // inside them, or they are neither read nor written
+        const long long q_total = __ldg(p.qo_indptr + p.batch);
+        const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
+        if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
+            q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
+            if (qp == 0 && g == 0 && tid == 0)
+                record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
+                                    : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
+            return;
+        }
+        rows = q_len * G;
+        P = kv_len - q_len;
+        lim_pos = kv_len - 1;
+    }
+    const int row0 = qp * 2 * kRows;
+    if (row0 >= rows || kv_end - kv_lo < 0) return;
+    // K/V tiles each query tile sees (0: the tile has no rows); B sees at least as many as A
 #pragma unroll
     for (int X = 0; X < 2; ++X) {
         const int rx = row0 + X * kRows;
         n_x[X] = 0;
         if (rx < rows) {
-            const int pos_last = (min(rx + kRows, rows) - 1) / G;
-            const int e = p.causal ? min(kv_len, P + pos_last + 1) : kv_len;
-            n_x[X] = (e + kTok - 1) / kTok;
-            kv_end = max(kv_end, e);
+            if constexpr (kGroup) {
+                n_x[X] = (kv_end - kv_lo + kTok - 1) / kTok;
+            } else {
+                const int pos_last = (min(rx + kRows, rows) - 1) / G;
+                const int e = p.causal ? min(lim_pos + 1, P + pos_last + 1) : lim_pos + 1;
+                n_x[X] = (e + kTok - 1) / kTok;
+                kv_end = max(kv_end, e);
+            }
         }
     }
-    const int n_tiles = max(n_x[0], n_x[1]);   // >= 1: kv_end >= 1 when rows > 0
+    const int n_tiles = max(n_x[0], n_x[1]);   // >= 1: kv_end > kv_lo when rows > 0
+    if (n_tiles == 0) return;                  // an empty chunk (not launched by the host)
 
     const int64_t slot_stride = static_cast<int64_t>(p.n_kv_heads) * kD;
     const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
     const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
     const int32_t *r2t = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len;
+    // slot of key position j (a page-table lookup in the group role when
+    // page_size > 0); a slot or page outside the pool is recorded and read as 0
+    auto slot_of = [&](int j) -> int {
+        if (kGroup && p.page_size > 0) {
+            const int pg = __ldg(p.req_to_page + static_cast<int64_t>(r) * p.max_pages + j / p.page_size);
+            if (static_cast<unsigned long long>(static_cast<long long>(pg)) >=
+                static_cast<unsigned long long>(p.n_pages)) {
+                record_error(p.err, pg);
+                return 0;
+            }
+            return pg * p.page_size + j % p.page_size;
+        }
+        int slot = __ldg(r2t + j);
+        if (static_cast<unsigned long long>(static_cast<long long>(slot)) >=
+            static_cast<unsigned long long>(p.size)) {
+            record_error(p.err, slot);
+            slot = 0;
+        }
+        return slot;
+    };
 
     // ---- setup: barriers, TMEM, the two query tiles
     if (tid == 0) {
@@ -286,20 +344,17 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-        // ================= producer: K and V tile t into ring slot t % 2
+    if (warp >= kSoftmaxWarps && warp < kMmaWarp && !kGroup) {
+        // ================= producer (prefill): K and V tile t into ring slot t % 2,
+        // through registers: the rows are mostly L2 hits here (each request's
+        // K/V is read by all its query-tile pairs), where this measured ~12%
+        // faster than the cp.async producer below
         const int pt = tid - kSoftmaxWarps * 32;
         int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
         auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
-            const int j = tile * kTok + pt;
+            const int j = kv_lo + tile * kTok + pt;
             if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
-            int slot = __ldg(r2t + j);
-            if (static_cast<unsigned long long>(static_cast<long long>(slot)) >=
-                static_cast<unsigned long long>(p.size)) {
-                record_error(p.err, slot);
-                slot = 0;
-            }
-            return slot;
+            return slot_of(j);
         };
         int slot_n = fetch(0);
         // A wait that gives up sets the abort flag; after that nothing is
@@ -341,6 +396,74 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 *s_abort = 1;
                 record_error(p.err, -2001);
             }
+        }
+    } else if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
+        // ================= producer (group role): K and V tile t into ring slot t % 2.
+        // The prefix rows come from DRAM while the private role streams at full
+        // bandwidth, so load latency dominates: 16-byte cp.async copies straight into the swizzled ring (no
+        // register round trip), so the copies of tile t are in flight while
+        // those of tile t - 1 land.  Commit groups go K(0), V(0), K(1), V(1),
+        // ...; once K(t) is committed, waiting until two groups remain means
+        // K(t - 1) has landed (likewise V), and the thread then makes its
+        // copies visible to the tensor core (proxy fence) and arrives on the
+        // slot's full barrier.  K(t) waits for its slot to be released by
+        // S(t - 2) and V(t) by P.V(t - 2), both of which the MMA thread can
+        // issue without K(t - 1) or V(t - 1): no wait here depends on an
+        // arrival that comes after it.
+        const int pt = tid - kSoftmaxWarps * 32;
+        int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
+        auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
+            const int j = kv_lo + tile * kTok + pt;
+            if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
+            return slot_of(j);
+        };
+        auto issue = [&](int X, int t) {   // X = 0: K, 1: V; rows past the range are zero-filled
+            const int *slots = s_slot + (t & 1) * kTok;
+            unsigned char *dst0 = sm + (X ? kSmemV : kSmemK) + (t & 1) * kTileBytes;
+            const bf16 *src0 = X ? vbase : kbase;
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) {
+                const int i = pt + k * kPT;
+                if (i < kTok * 16) {
+                    const int sl = slots[i >> 4];
+                    void *dst = dst0 + sw_chunk(i >> 4, i & 15);
+                    if (sl >= 0) cp_async16(dst, src0 + sl * slot_stride + (i & 15) * 8);
+                    else cp_async16(dst, src0, 0);
+                }
+            }
+            cp_async_commit();
+        };
+        auto publish = [&](int X, int t) {   // this thread's copies of tile t are complete
+            fence_async_smem();
+            mbar_arrive(bar((X ? kBarVFull : kBarKFull) + (t & 1)));
+        };
+        // A wait that gives up sets the abort flag; after that nothing is
+        // issued or published, but every producer barrier is still met.
+        int slot_n = fetch(0);
+        for (int t = 0; t < n_tiles; ++t) {
+            int *slots = s_slot + (t & 1) * kTok;
+            if (pt < kTok) slots[pt] = slot_n;
+            slot_n = fetch(t + 1);   // the next tile's index is in flight meanwhile
+            named_sync(1, kPT);      // this tile's slots are staged
+            bool live = *s_abort == 0 && bar_wait(bar(kBarKEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
+            if (live) issue(0, t);
+            else cp_async_commit();
+            cp_async_wait<2>();
+            if (live && t > 0) publish(0, t - 1);
+            live = live && bar_wait(bar(kBarVEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
+            if (live) issue(1, t);
+            else cp_async_commit();
+            cp_async_wait<2>();
+            if (live && t > 0) publish(1, t - 1);
+            if (!live && *s_abort == 0) {
+                *s_abort = 1;
+                record_error(p.err, -2001);
+            }
+        }
+        cp_async_wait<0>();
+        if (*s_abort == 0) {
+            publish(0, n_tiles - 1);
+            publish(1, n_tiles - 1);
         }
     } else if (warp == kMmaWarp) {
         // ================= MMA issue
@@ -410,6 +533,32 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         __syncwarp();
     } else {
         // ================= softmax: row `row`, columns [64 hc, 64 hc + 64) of each tile
+        if constexpr (kGroup) {
+            // The statement that the prefix is shared: every other entry of
+            // this CTA's rows must hold the first entry's table entries over
+            // the chunk (its page ids, or its slots through req_to_token).  The
+            // units to compare are split over the kv-head CTAs of the chunk; a
+            // mismatch is recorded as -100000 - b.  These warps would
+            // otherwise wait for the first scores.
+            const int HK = p.n_kv_heads;
+            const int b_lo = max(1, row0 / G), b_hi = min(p.batch, (row0 + 2 * kRows) / G);
+            const int ps = p.page_size;
+            const int u_lo = ps > 0 ? kv_lo / ps : kv_lo;
+            const int u_hi = ps > 0 ? (kv_end - 1) / ps + 1 : kv_end;
+            const int n_u = u_hi - u_lo > g ? (u_hi - u_lo - g + HK - 1) / HK : 0;
+            const int n_b = max(0, b_hi - b_lo);
+            const int32_t *tab = ps > 0 ? p.req_to_page : p.req_to_token;
+            const int64_t pitch = ps > 0 ? p.max_pages : p.max_ctx_len;
+            for (int i = tid; i < n_b * n_u; i += kSoftmaxWarps * 32) {
+                const int b = b_lo + i / n_u, u = u_lo + g + HK * (i % n_u);
+                const int rb = __ldg(p.req_pool_indices + b);
+                if (static_cast<unsigned>(rb) >= static_cast<unsigned>(p.num_reqs)) {
+                    record_error(p.err, rb);
+                    continue;
+                }
+                if (__ldg(tab + rb * pitch + u) != __ldg(tab + r * pitch + u)) record_error(p.err, -100000 - b);
+            }
+        }
         const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row of this thread
         const int hc = warp >> 2;                  // column half
         const int pair_bar = 2 + (warp & 3);       // named barrier of warps w and w + 4
@@ -420,7 +569,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
             const int R = row0 + X * kRows + row;
-            lim[X] = R < rows ? (p.causal ? P + R / G : kv_len - 1) : -1;   // last visible position
+            lim[X] = R < rows ? ((!kGroup && p.causal) ? P + R / G : lim_pos) : -1;   // last visible position
         }
         // A wait that gives up sets the abort flag; after that no wait is made,
         // but every named barrier is still met so the pair stays in step.
@@ -440,7 +589,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 wait_ok(bar(kBarSFull + X), j & 1);
                 fence_after();
                 const uint32_t tS = tmem + X * 256 + lane_off + hc * 64;
-                const int jt = j * kTok + hc * 64;
+                const int jt = kv_lo + j * kTok + hc * 64;
                 // this half's 64 scores, read once; masked only near the diagonal
                 float sv[64];
                 tmem_ld64(tS, sv);
@@ -521,25 +670,68 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             const int R = row0 + X * kRows + row;
             const int pos = R / G, hh = R - (R / G) * G;
-            bf16 *orow = static_cast<bf16 *>(p.o) +
-                         ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + hc * 64;
-            // every thread reads its lane (tcgen05.ld is warp-collective); rows
-            // past the request are not stored
+            const bool store = done && *s_abort == 0 && R < rows;
+            if constexpr (kGroup) {
+                // fp32 partial of entry pos, head g G + hh: o / l, then (m, l).
+                // The warp's 32 rows x 64 columns go through shared memory (the
+                // query and K tiles, whose last reader -- the final S product
+                // -- completed before this tile's O) so that global stores
+                // write whole 256-byte row pieces instead of one row per lane.
+                const uint64_t pol = l2_keep_policy();
+                float *stg = reinterpret_cast<float *>(sm + kSmemQ) + warp * 32 * kStgPitch;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float ov[32];
-                tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * 64 + c0, ov);
-                uint32_t pk[16];
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float ov[32];
+                    tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * 64 + c0, ov);
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
-                    pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        *reinterpret_cast<float4 *>(stg + lane * kStgPitch + c0 + 4 * q4) =
+                            make_float4(ov[4 * q4] * inv, ov[4 * q4 + 1] * inv, ov[4 * q4 + 2] * inv,
+                                        ov[4 * q4 + 3] * inv);
                 }
-                if (done && *s_abort == 0 && R < rows) {
+                __syncwarp();
+                if (done && *s_abort == 0) {
+                    // two rows per instruction, 16 lanes x 16 bytes each
+#pragma unroll 4
+                    for (int i = 0; i < 16; ++i) {
+                        const int rr = 2 * i + (lane >> 4), ch = lane & 15;
+                        const int Rr = row0 + X * kRows + (warp & 3) * 32 + rr;
+                        if (Rr < rows) {
+                            const int64_t unit_r = p.unit0 +
+                                (static_cast<int64_t>(chunk) * p.batch + Rr / G) * p.n_heads + g * G + Rr % G;
+                            const float4 v = *reinterpret_cast<const float4 *>(stg + rr * kStgPitch + ch * 4);
+                            st_keep4(p.o_part + unit_r * kD + hc * 64 + ch * 4, v.x, v.y, v.z, v.w, pol);
+                        }
+                    }
+                }
+                __syncwarp();   // the staging rows are rewritten for the next tile
+                if (store && hc == 0) {
+                    const int64_t unit =
+                        p.unit0 + (static_cast<int64_t>(chunk) * p.batch + pos) * p.n_heads + g * G + hh;
+                    st_keep(p.ml_part + unit * 2, m_run[X], pol);
+                    st_keep(p.ml_part + unit * 2 + 1, l_row, pol);
+                }
+            } else {
+                bf16 *orow = static_cast<bf16 *>(p.o) +
+                             ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + hc * 64;
+                // every thread reads its lane (tcgen05.ld is warp-collective); rows
+                // past the request are not stored
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        *reinterpret_cast<uint4 *>(orow + c0 + q4 * 8) =
-                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float ov[32];
+                    tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * 64 + c0, ov);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
+                        pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    if (store) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<uint4 *>(orow + c0 + q4 * 8) =
+                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    }
                 }
             }
         }
@@ -548,30 +740,98 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+    if constexpr (kGroup) {
+        // This grid was launched as a programmatic dependent of the decode's
+        // split kernel (the private role): it completes only after that one,
+        // so the merge, which waits for this grid, sees both roles' partials.
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    }
 }
 
-template <int G>
-cudaError_t run(const PrefillParams &p, cudaStream_t s) {
+template <int G, bool kGroup>
+cudaError_t set_smem_once() {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(prefill_tc_kernel<G, kGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
+    return cudaSuccess;
+}
+
+template <int G>
+cudaError_t run(const PrefillParams &p, cudaStream_t s) {
+    cudaError_t e = set_smem_once<G, false>();
+    if (e != cudaSuccess) return e;
     const int qtiles = (p.max_q_len * G + kRows - 1) / kRows;
     dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
-    prefill_tc_kernel<G><<<grid, kNT, kSmemBytes, s>>>(p);
+    prefill_tc_kernel<G, false><<<grid, kNT, kSmemBytes, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t run_group(const DecodeParams &d, cudaStream_t s) {
+    cudaError_t e = set_smem_once<G, true>();
+    if (e != cudaSuccess) return e;
+    PrefillParams p{};
+    p.q = d.q;
+    p.k_buffer = d.k_buffer;
+    p.v_buffer = d.v_buffer;
+    p.req_to_token = d.req_to_token;
+    p.req_pool_indices = d.req_pool_indices;
+    p.size = d.size;
+    p.layer_row0 = d.layer_row0;
+    p.n_kv_heads = d.n_kv_heads;
+    p.n_heads = d.n_heads;
+    p.num_reqs = d.num_reqs;
+    p.max_ctx_len = d.max_ctx_len;
+    p.batch = d.batch;
+    p.scale_log2 = d.scale_log2;
+    p.err = d.err;
+    p.req_to_page = d.req_to_page;
+    p.max_pages = d.max_pages;
+    p.page_size = d.page_size;
+    p.n_pages = d.n_pages;
+    p.shared_len = d.shared_len;
+    p.chunk_len = d.group_chunk_len;
+    p.o_part = d.o_part;
+    p.ml_part = d.ml_part;
+    p.unit0 = d.group_unit0;
+    const int row_blocks = (d.batch * G + kGroupRows - 1) / kGroupRows;
+    // a programmatic dependent of the split kernel: its CTAs start on the SMs
+    // the split kernel leaves free, without waiting for it to finish
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d.group_chunks, d.n_kv_heads, row_blocks);
+    cfg.blockDim = dim3(kNT);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G, true>, p);
 }
 
 }  // namespace
 
 bool prefill_tc_supported(int dtype, int head_dim, int group) {
     return dtype == PKV_BF16 && head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_t s) {
+    switch (group) {
+        case 1: return run_group<1>(p, s);
+        case 2: return run_group<2>(p, s);
+        case 4: return run_group<4>(p, s);
+        case 8: return run_group<8>(p, s);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, int group, cudaStream_t s) {

@@ -648,10 +648,11 @@ def shared_case(batch, heads, ps, shared, priv_hi, seed, d=128, hk=8):
                        shared_prefix=shared, seed=seed, rng=rng)
 
 
-def test_prefix_shared_decode_reads_the_shared_pages_once_per_group():
-    """The prefix-shared workload with its 128 shared pages stated: equal to
-    the oracle, and (another summation order) not bit-identical to the decode
-    that reads every request's prefix."""
+def test_prefix_shared_decode_reads_the_shared_pages_once():
+    """The prefix-shared workload with its 128 shared pages stated (read once
+    per launch, on the tensor cores): equal to the oracle, and (another
+    summation order) not bit-identical to the decode that reads every
+    request's prefix."""
     case = W.prefix_shared_decode()
     cache, q = prepare(case)
     ws = ws_for(case)
@@ -669,8 +670,10 @@ def test_prefix_shared_decode_reads_the_shared_pages_once_per_group():
     (9, 16, 4, 256, 64, 128),        # G = 2: groups of 8, page_size 4
     (5, 64, 32, 1024, 2000, 128),    # G = 8: pairs, long private tails
     (3, 32, 1, 64, 10, 128),         # single-slot pages, the shortest shared prefix used
-    (40, 32, 16, 4096, 50, 128),     # long prefix: many group CTAs per group
-    (20, 32, 16, 1024, 200, 64),     # head_dim 64
+    (40, 32, 16, 4096, 50, 128),     # long prefix: four chunks of 1024 positions
+    (70, 32, 16, 1008, 100, 128),    # 280 query rows: two row blocks; a partial last key tile
+    (24, 16, 4, 1500, 80, 128),      # two chunks, the last one ragged
+    (20, 32, 16, 1024, 200, 64),     # head_dim 64: the group role inside the split kernel
 ])
 def test_shared_prefix_variants(batch, heads, ps, shared, priv_hi, d):
     case = shared_case(batch, heads, ps, shared, priv_hi, seed=batch * 7 + ps, d=d)
@@ -757,12 +760,13 @@ def test_false_shared_prefix_claims_are_reported_not_faulted():
     assert st == _lib.PKV_ERR_INDEX
 
 
-@pytest.mark.parametrize("hk,shared_pages,splits", [(4, 32, 1024), (8, 3, 1024), (8, 32, 64)])
-def test_shared_prefix_statement_ignored_where_it_does_not_apply(hk, shared_pages, splits):
-    """4 kv heads, fewer than 64 shared positions, or a workspace without
-    room for the group partials: the decode runs as without the statement
-    (bit-identical)."""
-    case = shared_case(6, 4 * hk, 16, 512, 100, seed=88, hk=hk)
+@pytest.mark.parametrize("hk,shared_pages,splits,batch,d", [
+    (4, 32, 1024, 6, 128), (8, 3, 1024, 6, 128), (8, 32, 1024, 1, 128), (8, 32, 64, 6, 64)])
+def test_shared_prefix_statement_ignored_where_it_does_not_apply(hk, shared_pages, splits, batch, d):
+    """4 kv heads, fewer than 64 shared positions, a single entry, or (head_dim
+    64) a workspace without room for the group partials: the decode runs as
+    without the statement (bit-identical)."""
+    case = shared_case(batch, 4 * hk, 16, 512, 100, seed=88, hk=hk, d=d)
     cache, q = prepare(case)
     ws = ws_for(case, splits=splits)
     table = torch.from_numpy(page_table(case)).cuda()
