@@ -342,7 +342,9 @@ int pkv_paged_decode_noalloc(const pkv_kvcache *c, int32_t layer_id, const void 
  * recorded value: the offending slot, page, request row, length or position
  * itself, or one of these codes:
  *   -1000 - k      a decode wait on the copies of stage k gave up;
- *   -2001, -2007   a prefill wait (producer, tensor-core thread) gave up;
+ *   -2001, -2007   a prefill wait gave up (producer, softmax warps);
+ *   -3002 .. -3006 a prefill wait of the thread issuing tensor-core
+ *                  instructions gave up;
  *   -100000 - b    a shared prefix was stated, but entry b's leading pages (or
  *                  slots) differ from those of its group's first entry;
  *   -200000 - c    shared-prefix CTA c was handed more positions than it
