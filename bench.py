@@ -798,7 +798,29 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
             "rope_kv_write_frac_of_hbm": round(rb / (t_rope * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "ms_per_step": round(statistics.mean(ms), 4),
             "timing": {"prefill": tstats(parts[1]), "kv_write": tstats(parts[0]),
-                       "rope_kv_write": tstats(ms_r)}}
+                       "rope_kv_write": tstats(ms_r)},
+            "head_dim_64": prefill_d64_leg(torch, pkv, W, stream, flush, peaks, args, dev)}
+
+
+def prefill_d64_leg(torch, pkv, W, stream, flush, peaks, args, dev):
+    """The same ragged causal prefill shape at head_dim 64 (the tcgen05 kernel's
+    head_dim-64 instantiation)."""
+    case = W.ragged_prefill(head_dim=64)
+    cache, q, kn, vn = W.upload(case, dev)
+    pkv.kv_write(cache, case.layer_id, kn, vn, stream=stream)
+    o = torch.empty_like(q)
+    with torch.cuda.stream(stream):
+        ms, _ = timed(torch, stream, lambda: pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len,
+                                                              case.max_len, o=o, stream=stream),
+                      args.prefill_steps, 3, flush)
+    st, detail = pkv.last_device_error(stream, dev)
+    if st != 0:
+        raise RuntimeError(f"device error word set in the head_dim 64 prefill (detail {detail})")
+    t = statistics.mean(ms)
+    fl = prefill_flops(case)
+    tf = fl / (t * 1e-3) / 1e12
+    return {"causal_flops": fl, "ms_prefill": round(t, 4), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "timing": tstats(ms)}
 
 
 def allocator_leg():

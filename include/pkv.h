@@ -301,9 +301,8 @@ int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *
  * sizing).  An entry whose rows [qo_indptr[b], qo_indptr[b+1]) do not lie
  * within [0, qo_indptr[batch]), or whose lengths break these bounds, is a
  * device-data error: its rows of q and o are neither read nor written.
- * `ws` may be NULL.  Supported: bf16, head_dim 128 (5th-generation
- * tensor cores, accumulators in tensor memory) or 64 (mma.sync), G in
- * {1, 2, 4, 8}.
+ * `ws` may be NULL.  Supported: bf16, head_dim 64 or 128 (5th-generation
+ * tensor cores, accumulators in tensor memory), G in {1, 2, 4, 8}.
  */
 int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
                       int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,

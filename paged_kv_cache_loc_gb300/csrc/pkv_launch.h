@@ -158,10 +158,9 @@ bool decode_balanced_supported(int dtype, int head_dim, int group, int n_kv_head
 cudaError_t launch_decode_merge_balanced(const DecodeParams &p, int head_dim, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group,
                            cudaStream_t s);
+// The prefill runs on tcgen05 with accumulators in TMEM for bf16 head_dim 64
+// and 128 (pkv_prefill_tc.cu).
 bool prefill_supported(int dtype, int head_dim, int group);
-// tcgen05 (TMEM) prefill for bf16 head_dim 128 (pkv_prefill_tc.cu).
-bool prefill_tc_supported(int dtype, int head_dim, int group);
-cudaError_t launch_prefill_tc(const PrefillParams &p, int group, cudaStream_t s);
 // The shared-prefix group role of a decode with p.group_tc set
 // (pkv_prefill_tc.cu); launched before the split kernel.
 cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_t s);

@@ -1,11 +1,14 @@
 // pkv_prefill_tc.cu -- ragged paged prefill on the 5th-generation tensor cores
-// (tcgen05, accumulators in tensor memory), bf16, head_dim 128.
+// (tcgen05, accumulators in tensor memory), bf16, head_dim 64 or 128; the same
+// pipeline runs the group role of the shared-prefix decode (head_dim 128).
 //
-// Operation: as in pkv_prefill.cu (AstrAI docs/guides/inference.md,
-// "Attention Backend" prefill path; causal alignment from
-// astrai/model/transformer.py process_attention_mask): packed query row
-// qo_indptr[b] + i, head h attends to slots req_to_token[req_pool_indices[b], j]
-// for j <= P + i (P = kv_len - q_len) or j < kv_len when not causal.
+// Operation (AstrAI docs/guides/inference.md, "Attention Backend" prefill
+// path; causal alignment from astrai/model/transformer.py
+// process_attention_mask): entry b has q_len = qo_indptr[b+1] - qo_indptr[b]
+// new tokens at the end of kv_len = kv_indptr[b+1] - kv_indptr[b] positions;
+// packed query row qo_indptr[b] + i, head h attends to slots
+// req_to_token[req_pool_indices[b], j] of kv head h / G for j <= P + i
+// (P = kv_len - q_len) or j < kv_len when not causal.
 //
 // One CTA of 16 warps per (pair of query tiles, kv head, entry).  A query
 // tile is 128 rows of (position, head-in-group) pairs; the CTA's two tiles A
@@ -15,13 +18,15 @@
 // this kernel.  The warps specialise and hand work over through mbarriers
 // (every wait bounded):
 //  - producer warps 8..14 (224 threads): each 128-token K and V tile is
-//    loaded with 16-byte loads (16 threads per 256-byte token row, slot
+//    loaded with 16-byte loads (head_dim / 8 threads per token row, slot
 //    indices staged in shared memory) into registers, then stored into a
-//    2-slot ring once the tensor core has released the slot;
+//    2-slot ring once the tensor core has released the slot (the group role
+//    copies with cp.async instead, see its producer);
 //  - MMA warp 15 (one thread) issues, per tile j,
 //      PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)     (S = Q K^T, O += P V),
-//    each of 8 tcgen05.mma (M=128, N=128, K=16), so the tensor core works on
-//    one query tile while the softmax runs on the other;
+//    S as head_dim / 16 tcgen05.mma (M=128, N=128, K=16) and P.V as 8
+//    (M=128, N=head_dim, K=16), so the tensor core works on one query tile
+//    while the softmax runs on the other;
 //  - softmax warps 0..7: warps w and w+4 share TMEM lanes 32(w%4).. and take
 //    one 64-column half of each row.  A thread reads its 64 scores of S_X(j)
 //    into registers once, exchanges its half's maximum with the other half
@@ -31,10 +36,11 @@
 //    complete, as it was issued before S_X(j)), and stores P = 2^(s - m) as
 //    bf16 pairs over the S columns it has read; P.V reads P from TMEM as its
 //    A operand.
-// TMEM (512 columns): tile X in {A, B} has S (and P) at 256 X and O at
-// 256 X + 128.  Q, K and V tiles use the 128-byte swizzle: a [rows x 128]
-// bf16 tile is two 64-column halves of rows x 128 B, 16-byte chunk c of row
-// r stored at chunk c ^ (r % 8), atoms 1024-byte aligned.
+// TMEM (512 columns): tile X in {A, B} has S (and P) at 256 X and O (head_dim
+// columns) at 256 X + 128.  Q, K and V tiles use the 128-byte swizzle: a
+// [rows x head_dim] bf16 tile is one or two 64-column halves of rows x 128 B,
+// 16-byte chunk c of row r stored at chunk c ^ (r % 8), atoms 1024-byte
+// aligned.
 #include <atomic>
 
 #include "pkv_common.cuh"
@@ -45,18 +51,11 @@ namespace {
 
 constexpr int kRows = 128;       // query rows per query tile (TMEM lanes)
 constexpr int kTok = 128;        // kv tokens per tile
-constexpr int kD = 128;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarps = 7;
 constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
 constexpr int kNT = (kMmaWarp + 1) * 32;                   // 512 threads
 constexpr int kPT = kProducerWarps * 32;                   // 224 producer threads
-constexpr int kChunks = (kTok * 16 + kPT - 1) / kPT;       // 16-byte chunks per producer thread and tile
-constexpr int kTileBytes = 128 * 128 * 2;                  // 32 KB: any [128 x 128] bf16 tile
-constexpr int kSmemQ = 0;                                  // [2] query tiles A, B
-constexpr int kSmemK = 2 * kTileBytes;                     // [2] K slots
-constexpr int kSmemV = kSmemK + 2 * kTileBytes;            // [2] V slots
-constexpr int kSmemBar = kSmemV + 2 * kTileBytes;
 // mbarriers
 constexpr int kBarKFull = 0;     // [2 slots] count kPT: producer threads
 constexpr int kBarKEmpty = 2;    // [2 slots] count 1: commit after the tile's S products
@@ -66,22 +65,38 @@ constexpr int kBarSFull = 8;     // [2 query tiles] count 1: S_X(j) complete
 constexpr int kBarPFull = 10;    // [2 query tiles] count 8: softmax warps have stored P_X(j)
 constexpr int kBarODone = 12;    // [2 query tiles] count 1: the last P.V_X complete
 constexpr int kNumBars = 14;
-constexpr int kSmemTmemAddr = kSmemBar + kNumBars * 8;
-constexpr int kSmemAbort = kSmemTmemAddr + 4;
-constexpr int kSmemRed = kSmemBar + 256;                   // [2 tiles][2 buffers][2 halves][kRows] float
-constexpr int kSmemSlots = kSmemRed + 2 * 2 * 2 * kRows * 4;   // [2][kTok] int: producer's slot indices
-constexpr int kSmemBytes = kSmemSlots + 2 * kTok * 4 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescale = 8.f;                            // lazy rescale threshold (log2 units)
-static_assert(kSmemAbort + 4 <= kSmemRed, "barrier area");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 static_assert(kGroupRows == 2 * kRows, "a group-role CTA holds two query tiles");
 // group-role epilogue: each softmax warp stages 32 rows x 64 fp32 columns with
 // a 16-byte row pad (conflict-free 16-byte stores) in the query + K tile area
 constexpr int kStgPitch = 68;
-static_assert(kSoftmaxWarps * 32 * kStgPitch * 4 <= kSmemV - kSmemQ, "epilogue staging fits the Q and K tiles");
 
-// byte offset of 16-byte chunk `ch` (0..15) of row r
+// Shared-memory layout for head_dim D (64 or 128): Q, K and V tiles are
+// [128 x D] bf16 (one or two 128-byte-swizzled 64-column halves).
+template <int D>
+struct TcLayout {
+    static constexpr int kChunksRow = D / 8;                          // 16-byte chunks per row
+    static constexpr int kChunks = (kTok * kChunksRow + kPT - 1) / kPT;   // per producer thread and tile
+    static constexpr int kTileBytes = 128 * D * 2;                    // any [128 x D] bf16 tile
+    static constexpr int kSmemQ = 0;                                  // [2] query tiles A, B
+    static constexpr int kSmemK = 2 * kTileBytes;                     // [2] K slots
+    static constexpr int kSmemV = kSmemK + 2 * kTileBytes;            // [2] V slots
+    static constexpr int kSmemBar = kSmemV + 2 * kTileBytes;
+    static constexpr int kSmemTmemAddr = kSmemBar + kNumBars * 8;
+    static constexpr int kSmemAbort = kSmemTmemAddr + 4;
+    static constexpr int kSmemRed = kSmemBar + 256;                   // [2 tiles][2 buffers][2 halves][kRows] float
+    static constexpr int kSmemSlots = kSmemRed + 2 * 2 * 2 * kRows * 4;   // [2][kTok] int: producer's slot indices
+    static constexpr int kSmemBytes = kSmemSlots + 2 * kTok * 4 + 1024;   // + alignment slack
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(kSmemAbort + 4 <= kSmemRed, "barrier area");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+static_assert(kSoftmaxWarps * 32 * kStgPitch * 4 <= TcLayout<128>::kSmemV - TcLayout<128>::kSmemQ,
+              "epilogue staging fits the Q and K tiles");
+
+// byte offset of 16-byte chunk `ch` (0..15, or 0..7 for head_dim 64) of row r
+// of a 128-row tile
 __device__ __forceinline__ uint32_t sw_chunk(int r, int ch) {
     return (ch >> 3) * (128 * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
@@ -205,9 +220,15 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
 // keys are the chunk's positions of the first entry's request row, nothing is
 // masked, and the CTA ends with fp32 partials (o / l and (m, l)) that the
 // decode's merge folds in.  Both share the pipeline below.
-template <int G, bool kGroup>
+template <int G, bool kGroup, int D>
 __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams p) {
     using bf16 = __nv_bfloat16;
+    using L = TcLayout<D>;
+    static_assert(!kGroup || D == 128, "the shared-prefix group role runs at head_dim 128");
+    constexpr int kCR = L::kChunksRow, kChunks = L::kChunks, kTileBytes = L::kTileBytes;
+    constexpr int kSmemQ = L::kSmemQ, kSmemK = L::kSmemK, kSmemV = L::kSmemV, kSmemBar = L::kSmemBar;
+    constexpr int kSmemTmemAddr = L::kSmemTmemAddr, kSmemAbort = L::kSmemAbort, kSmemRed = L::kSmemRed;
+    constexpr int kSmemSlots = L::kSmemSlots;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t s_base = smem_u32(sm);
@@ -280,9 +301,9 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     const int n_tiles = max(n_x[0], n_x[1]);   // >= 1: kv_end > kv_lo when rows > 0
     if (n_tiles == 0) return;                  // an empty chunk (not launched by the host)
 
-    const int64_t slot_stride = static_cast<int64_t>(p.n_kv_heads) * kD;
-    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
-    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + (p.layer_row0 * p.n_kv_heads + g) * kD;
+    const int64_t slot_stride = static_cast<int64_t>(p.n_kv_heads) * D;
+    const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + (p.layer_row0 * p.n_kv_heads + g) * D;
+    const bf16 *vbase = static_cast<const bf16 *>(p.v_buffer) + (p.layer_row0 * p.n_kv_heads + g) * D;
     const int32_t *r2t = p.req_to_token + static_cast<int64_t>(r) * p.max_ctx_len;
     // slot of key position j (a page-table lookup in the group role when
     // page_size > 0); a slot or page outside the pool is recorded and read as 0
@@ -324,13 +345,13 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     }
     {
         const bf16 *q = static_cast<const bf16 *>(p.q);
-        for (int i = tid; i < 2 * kRows * 16; i += kNT) {
-            const int X = i / (kRows * 16), rr = (i >> 4) & (kRows - 1), ch = i & 15;
+        for (int i = tid; i < 2 * kRows * kCR; i += kNT) {
+            const int X = i / (kRows * kCR), rr = (i / kCR) & (kRows - 1), ch = i % kCR;
             const int Rq = row0 + X * kRows + rr;
             void *dst = sm + kSmemQ + X * kTileBytes + sw_chunk(rr, ch);
             if (Rq < rows) {
                 const int pos = Rq / G, hh = Rq - (Rq / G) * G;
-                cp_async16(dst, q + ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + ch * 8);
+                cp_async16(dst, q + ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * D + ch * 8);
             } else {
                 cp_async16(dst, q, 0);
             }
@@ -369,10 +390,10 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             for (int k = 0; k < kChunks; ++k) {
                 const int i = pt + k * kPT;
                 kv[0][k] = kv[1][k] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < kTok * 16) {
-                    const int sl = slots[i >> 4];
+                if (i < kTok * kCR) {
+                    const int sl = slots[i / kCR];
                     if (sl >= 0) {
-                        const int64_t off = sl * slot_stride + (i & 15) * 8;
+                        const int64_t off = sl * slot_stride + (i % kCR) * 8;
                         kv[0][k] = __ldcg(reinterpret_cast<const uint4 *>(kbase + off));
                         kv[1][k] = __ldcg(reinterpret_cast<const uint4 *>(vbase + off));
                     }
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
 #pragma unroll
                 for (int k = 0; k < kChunks; ++k) {
                     const int i = pt + k * kPT;
-                    if (i < kTok * 16) *reinterpret_cast<uint4 *>(dst0 + sw_chunk(i >> 4, i & 15)) = kv[X][k];
+                    if (i < kTok * kCR) *reinterpret_cast<uint4 *>(dst0 + sw_chunk(i / kCR, i % kCR)) = kv[X][k];
                 }
                 fence_async_smem();   // these generic stores -> the tensor core's reads
                 mbar_arrive(bar((X ? kBarVFull : kBarKFull) + (t & 1)));
@@ -424,10 +445,10 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
 #pragma unroll
             for (int k = 0; k < kChunks; ++k) {
                 const int i = pt + k * kPT;
-                if (i < kTok * 16) {
-                    const int sl = slots[i >> 4];
-                    void *dst = dst0 + sw_chunk(i >> 4, i & 15);
-                    if (sl >= 0) cp_async16(dst, src0 + sl * slot_stride + (i & 15) * 8);
+                if (i < kTok * kCR) {
+                    const int sl = slots[i / kCR];
+                    void *dst = dst0 + sw_chunk(i / kCR, i % kCR);
+                    if (sl >= 0) cp_async16(dst, src0 + sl * slot_stride + (i % kCR) * 8);
                     else cp_async16(dst, src0, 0);
                 }
             }
@@ -468,12 +489,12 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     } else if (warp == kMmaWarp) {
         // ================= MMA issue
         if (lane == 0) {
-            const uint32_t id_s = idesc(128, 128, 0), id_o = idesc(128, 128, 1);
+            const uint32_t id_s = idesc(128, 128, 0), id_o = idesc(128, D, 1);
             auto issue_s = [&](int X, int slot) {   // S_X = Q_X K^T
                 const uint32_t qaddr = s_base + kSmemQ + X * kTileBytes;
                 const uint32_t kaddr = s_base + kSmemK + slot * kTileBytes;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
                     mma_f16(tmem + X * 256, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + off, 16, 1024), id_s,
                             ks > 0);
@@ -617,9 +638,9 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 const bool touch_o = raise && j > 0 && m_run[X] != -INFINITY;
                 if (__any_sync(0xffffffffu, touch_o)) {
                     const float f = touch_o ? alpha : 1.f;
-                    const uint32_t tO = tmem + X * 256 + 128 + lane_off + hc * 64;
+                    const uint32_t tO = tmem + X * 256 + 128 + lane_off + hc * (D / 2);
 #pragma unroll 1
-                    for (int h2 = 0; h2 < 2; ++h2) {   // one 32-column piece at a time: sv stays live
+                    for (int h2 = 0; h2 < D / 64; ++h2) {   // one 32-column piece at a time: sv stays live
                         float v[32];
                         tmem_ld32(tO + h2 * 32, v);
 #pragma unroll
@@ -700,7 +721,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                             const int64_t unit_r = p.unit0 +
                                 (static_cast<int64_t>(chunk) * p.batch + Rr / G) * p.n_heads + g * G + Rr % G;
                             const float4 v = *reinterpret_cast<const float4 *>(stg + rr * kStgPitch + ch * 4);
-                            st_keep4(p.o_part + unit_r * kD + hc * 64 + ch * 4, v.x, v.y, v.z, v.w, pol);
+                            st_keep4(p.o_part + unit_r * D + hc * 64 + ch * 4, v.x, v.y, v.z, v.w, pol);
                         }
                     }
                 }
@@ -713,13 +734,13 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 }
             } else {
                 bf16 *orow = static_cast<bf16 *>(p.o) +
-                             ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * kD + hc * 64;
+                             ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * D + hc * (D / 2);
                 // every thread reads its lane (tcgen05.ld is warp-collective); rows
                 // past the request are not stored
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     float ov[32];
-                    tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * 64 + c0, ov);
+                    tmem_ld32(tmem + X * 256 + 128 + lane_off + hc * (D / 2) + c0, ov);
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
@@ -748,7 +769,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     }
 }
 
-template <int G, bool kGroup>
+template <int G, bool kGroup, int D>
 cudaError_t set_smem_once() {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
@@ -756,27 +777,38 @@ cudaError_t set_smem_once() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<G, kGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        e = cudaFuncSetAttribute(prefill_tc_kernel<G, kGroup, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcLayout<D>::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
     return cudaSuccess;
 }
 
-template <int G>
+template <int G, int D>
 cudaError_t run(const PrefillParams &p, cudaStream_t s) {
-    cudaError_t e = set_smem_once<G, false>();
+    cudaError_t e = set_smem_once<G, false, D>();
     if (e != cudaSuccess) return e;
     const int qtiles = (p.max_q_len * G + kRows - 1) / kRows;
     dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
-    prefill_tc_kernel<G, false><<<grid, kNT, kSmemBytes, s>>>(p);
+    prefill_tc_kernel<G, false, D><<<grid, kNT, TcLayout<D>::kSmemBytes, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_d(const PrefillParams &p, int group, cudaStream_t s) {
+    switch (group) {
+        case 1: return run<1, D>(p, s);
+        case 2: return run<2, D>(p, s);
+        case 4: return run<4, D>(p, s);
+        case 8: return run<8, D>(p, s);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 template <int G>
 cudaError_t run_group(const DecodeParams &d, cudaStream_t s) {
-    cudaError_t e = set_smem_once<G, true>();
+    cudaError_t e = set_smem_once<G, true, 128>();
     if (e != cudaSuccess) return e;
     PrefillParams p{};
     p.q = d.q;
@@ -808,20 +840,27 @@ cudaError_t run_group(const DecodeParams &d, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.group_chunks, d.n_kv_heads, row_blocks);
     cfg.blockDim = dim3(kNT);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = TcLayout<128>::kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G, true>, p);
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G, true, 128>, p);
 }
 
 }  // namespace
 
-bool prefill_tc_supported(int dtype, int head_dim, int group) {
-    return dtype == PKV_BF16 && head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8);
+bool prefill_supported(int dtype, int head_dim, int group) {
+    return dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group, cudaStream_t s) {
+    if (!prefill_supported(dtype, head_dim, group)) return cudaErrorNotSupported;
+    if (p.batch == 0 || p.max_q_len == 0) return cudaSuccess;
+    return head_dim == 128 ? run_d<128>(p, group, s) : run_d<64>(p, group, s);
 }
 
 cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_t s) {
@@ -830,16 +869,6 @@ cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_
         case 2: return run_group<2>(p, s);
         case 4: return run_group<4>(p, s);
         case 8: return run_group<8>(p, s);
-        default: return cudaErrorNotSupported;
-    }
-}
-
-cudaError_t launch_prefill_tc(const PrefillParams &p, int group, cudaStream_t s) {
-    switch (group) {
-        case 1: return run<1>(p, s);
-        case 2: return run<2>(p, s);
-        case 4: return run<4>(p, s);
-        case 8: return run<8>(p, s);
         default: return cudaErrorNotSupported;
     }
 }

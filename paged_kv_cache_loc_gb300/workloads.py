@@ -259,15 +259,17 @@ def prefix_shared_decode(batch: int = 64, prefix: int = 2048, private_hi: int = 
 
 
 def ragged_prefill(batch: int = 16, q_lo: int = 128, q_hi: int = 2048, p_hi: int = 4096,
-                   size: int = 131072, seed: int = 1005, causal: bool = True) -> Case:
+                   size: int = 131072, seed: int = 1005, causal: bool = True,
+                   head_dim: int = 128) -> Case:
     """Ragged causal prefill: 16 requests, q_len uniform in [128, 2048], cached
-    prefix uniform in [0, 4096], kv_len = prefix + q_len, bf16, permuted slots."""
+    prefix uniform in [0, 4096], kv_len = prefix + q_len, bf16, permuted slots
+    (head_dim 128 unless stated)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     ql = rng.integers(q_lo, q_hi, size=batch, endpoint=True)
     pre = rng.integers(0, p_hi, size=batch, endpoint=True)
     kv = pre + ql
     return make_case(f"ragged_prefill_b{batch}", mode="prefill", dtype="bf16", n_layers=4,
-                     layer_id=2, size=size, n_heads=32, n_kv_heads=8, head_dim=128,
+                     layer_id=2, size=size, n_heads=32, n_kv_heads=8, head_dim=head_dim,
                      kv_lens=kv, q_lens=ql, seed=seed, max_ctx_len=int(kv.max()),
                      causal=causal, rng=rng)
 

@@ -152,9 +152,9 @@ def run_prefill(case, causal=True):
     return cache, q, o
 
 
-@pytest.mark.parametrize("causal", [True, False])
-def test_ragged_prefill_reduced_full_check(causal):
-    case = W.ragged_prefill(batch=4, q_lo=1, q_hi=256, p_hi=512, size=8192, seed=2005)
+@pytest.mark.parametrize("causal,d", [(True, 128), (False, 128), (True, 64), (False, 64)])
+def test_ragged_prefill_reduced_full_check(causal, d):
+    case = W.ragged_prefill(batch=4, q_lo=1, q_hi=256, p_hi=512, size=8192, seed=2005, head_dim=d)
     _, _, o = run_prefill(case, causal)
     ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
                          case.qo_indptr, case.kv_indptr, case.q, case.layer_id, causal=causal)
@@ -199,7 +199,8 @@ def test_decode_variants_and_ragged_lengths(dtype, heads, hk, d):
         assert_close(got, ref, dtype, f"chunk {chunk}")
 
 
-@pytest.mark.parametrize("heads,hk,d", [(8, 8, 128), (16, 8, 128), (64, 8, 128), (32, 8, 64)])
+@pytest.mark.parametrize("heads,hk,d", [(8, 8, 128), (16, 8, 128), (64, 8, 128), (8, 8, 64), (16, 8, 64),
+                                         (32, 8, 64), (64, 8, 64)])
 def test_prefill_variants(heads, hk, d):
     q_lens = [0, 1, 5, 64, 65, 130]
     pre = [7, 0, 100, 0, 63, 1]
