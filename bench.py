@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--decode-sweep", action="store_true",
                     help="print decode KV GB/s over batch x context (uniform contexts) and exit")
-    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "kvwrite", "prefix_shared"],
+    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "prefill64", "kvwrite",
+                                               "prefix_shared"],
                     help="run a few untimed calls of one kernel's case (for ncu) and exit")
     return ap.parse_args()
 
@@ -107,7 +108,8 @@ def run_decode_sweep() -> None:
 def run_profile_case(which: str) -> None:
     """A few untimed calls of one workload, sized for an ncu capture (a few GB
     on the device at most): decode = the batched decode (98,304-slot pool),
-    long = B=1 at 32,768 tokens, prefill = 4 ragged-prefill requests,
+    long = B=1 at 32,768 tokens, prefill = 4 ragged-prefill requests (prefill64:
+    the same at head_dim 64),
     kvwrite = the ragged prefill's cache write (17,418 tokens), prefix_shared =
     the prefix-shared workload through the page table with its 128 shared
     pages stated."""
@@ -136,8 +138,8 @@ def run_profile_case(which: str) -> None:
         for _ in range(3):
             pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, o, workspace=ws,
                                    shared_pages=case.shared_prefix // ps)
-    elif which == "prefill":
-        case = W.ragged_prefill(batch=4, size=32768)
+    elif which in ("prefill", "prefill64"):
+        case = W.ragged_prefill(batch=4, size=32768, head_dim=64 if which == "prefill64" else 128)
         cache, q, kn, vn = W.upload(case)
         pkv.kv_write(cache, case.layer_id, kn, vn)
         o = torch.empty_like(q)

@@ -208,12 +208,13 @@ int pkv_paged_decode(const pkv_kvcache *c, int32_t layer_id, const void *q, void
  * prefix cache ("KVCache System") hands several tasks the same pages.  Same
  * operation and result as pkv_paged_decode; with the balanced plan, 8 kv
  * heads, shared_len >= 64, batch >= 2 and room in the workspace the shared
- * rows are read once per group of 16 / G requests (see
- * pkv_paged_decode_pages for the workspace it needs), otherwise the
- * statement is ignored.  Every seq_len must be >= shared_len; a shorter
- * context, or a row whose leading slots differ from its group's, is a
- * device-data error.  shared_len < 0, or shared_len > c->max_len, returns
- * PKV_ERR_ARG.
+ * rows are read once per launch at head_dim 128 and once per group of 16 / G
+ * requests at head_dim 64 (see pkv_paged_decode_pages for how, and for the
+ * workspace it needs), otherwise the statement is ignored.  Every seq_len
+ * must be >= shared_len; a shorter context, or a row whose leading slots
+ * differ from the first entry's (head_dim 128) or its group's (head_dim
+ * 64), is a device-data error.  shared_len < 0, or shared_len > c->max_len,
+ * returns PKV_ERR_ARG.
  */
 int pkv_paged_decode_shared(const pkv_kvcache *c, int32_t layer_id, int32_t shared_len,
                             const void *q, void *o, int32_t n_heads, float sm_scale,
@@ -239,14 +240,23 @@ int pkv_paged_decode_shared(const pkv_kvcache *c, int32_t layer_id, int32_t shar
  * every row of the batch are the same pages (a prefix shared by all
  * requests, "KVCache System" prefix cache hits); 0 states nothing.  It does
  * not change the result: with 8 kv heads, at least 64 shared positions
- * (shared_pages * page_size), batch >= 2 and room in the workspace it lets
- * the decode read each shared K/V row once per group of 16 / G requests
- * instead of once per request, and merge the two parts (the workspace then
- * holds (CTAs + batch) x n_heads rows plus (CTAs + ceil(batch / (16 / G)))
- * x (16 / G) x n_heads more); otherwise it is ignored.  Every seq_len must
- * be >= shared_pages * page_size; a shorter context, or a row whose leading
- * pages differ from its group's, is a device-data error.  shared_pages < 0,
- * or shared positions beyond c->max_len, returns PKV_ERR_ARG.
+ * (Ts = shared_pages * page_size), batch >= 2 and room in the workspace it
+ * lets the decode read each shared K/V row fewer times than once per
+ * request, and merge the two parts; otherwise it is ignored.
+ *   - head_dim 128: once per launch.  A tensor-core kernel attends all
+ *     batch x G query heads of each kv head to the prefix (read from the
+ *     first entry's row) in chunks of at most 512 positions, one CTA per
+ *     (chunk, kv head, 256 query rows), while the split kernel takes every
+ *     entry's positions past the prefix on the other SMs.  The workspace
+ *     then holds (CTAs + batch) x n_heads rows plus ceil(Ts / 512) x batch x
+ *     n_heads more, CTAs being the SM count minus the tensor-core kernel's.
+ *   - head_dim 64: once per group of 16 / G consecutive requests, inside the
+ *     split kernel; the workspace holds (CTAs + batch) x n_heads rows plus
+ *     (CTAs + ceil(batch / (16 / G))) x (16 / G) x n_heads more.
+ * Every seq_len must be >= Ts; a shorter context, or a row whose leading
+ * pages differ from the first entry's (head_dim 128) or its group's
+ * (head_dim 64), is a device-data error.  shared_pages < 0, or shared
+ * positions beyond c->max_len, returns PKV_ERR_ARG.
  */
 int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t *req_to_page,
                            int32_t max_pages, int32_t page_size, int32_t shared_pages,
@@ -345,7 +355,8 @@ int pkv_paged_decode_noalloc(const pkv_kvcache *c, int32_t layer_id, const void 
  *   -3002 .. -3006 a prefill wait of the thread issuing tensor-core
  *                  instructions gave up;
  *   -100000 - b    a shared prefix was stated, but entry b's leading pages (or
- *                  slots) differ from those of its group's first entry;
+ *                  slots) differ from the first entry's (head_dim 128) or
+ *                  from its group's first entry's (head_dim 64);
  *   -200000 - c    shared-prefix CTA c was handed more positions than it
  *                  stages (not expected: the host sizes the grid for it).
  * An offending value can itself be negative (a negative slot, say).
