@@ -53,8 +53,8 @@ def parse_args():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--decode-sweep", action="store_true",
                     help="print decode KV GB/s over batch x context (uniform contexts) and exit")
-    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "prefill64", "kvwrite",
-                                               "prefix_shared"],
+    ap.add_argument("--profile-case", choices=["decode", "long", "prefill", "prefill64", "prefill_full",
+                                               "kvwrite", "prefix_shared"],
                     help="run a few untimed calls of one kernel's case (for ncu) and exit")
     return ap.parse_args()
 
@@ -109,7 +109,7 @@ def run_profile_case(which: str) -> None:
     """A few untimed calls of one workload, sized for an ncu capture (a few GB
     on the device at most): decode = the batched decode (98,304-slot pool),
     long = B=1 at 32,768 tokens, prefill = 4 ragged-prefill requests (prefill64:
-    the same at head_dim 64),
+    the same at head_dim 64; prefill_full: the whole ragged-prefill workload, ~2.2 GB),
     kvwrite = the ragged prefill's cache write (17,418 tokens), prefix_shared =
     the prefix-shared workload through the page table with its 128 shared
     pages stated."""
@@ -138,8 +138,9 @@ def run_profile_case(which: str) -> None:
         for _ in range(3):
             pkv.paged_decode_pages(cache, case.layer_id, table, ps, q, o, workspace=ws,
                                    shared_pages=case.shared_prefix // ps)
-    elif which in ("prefill", "prefill64"):
-        case = W.ragged_prefill(batch=4, size=32768, head_dim=64 if which == "prefill64" else 128)
+    elif which in ("prefill", "prefill64", "prefill_full"):
+        case = (W.ragged_prefill() if which == "prefill_full" else
+                W.ragged_prefill(batch=4, size=32768, head_dim=64 if which == "prefill64" else 128))
         cache, q, kn, vn = W.upload(case)
         pkv.kv_write(cache, case.layer_id, kn, vn)
         o = torch.empty_like(q)
@@ -792,7 +793,9 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
             "tflops": round(tf, 1), "roofline": {
                 "bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["bf16_source"]},
+                "peak_source": peaks["bf16_source"],
+                "traffic": profile_traffic("prefill_tc_ragged.md", "pkv_prefill_tc.cu"),
+                "traffic_note": "DRAM bytes read + written per launch of the whole workload, from the committed ncu summary"},
             "kv_write_ms": round(t_wr, 4), "kv_write_gbs": round(wb / (t_wr * 1e-3) / 1e9, 1),
             "kv_write_frac_of_hbm": round(wb / (t_wr * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "rope_kv_write_ms": round(t_rope, 4),
