@@ -85,44 +85,71 @@ __device__ __forceinline__ uint4 rotate_chunk_f32(uint4 x, const float *cs) {
                       __float_as_uint(re1 * c.z - im1 * c.w), __float_as_uint(re1 * c.w + im1 * c.z));
 }
 
+// The fused write: the first k_blocks CTAs rotate K, one thread per (token,
+// chunk offset within a head) for every kv head of the token, so the chunk's
+// cos/sin pairs are read once for all heads (a table row would otherwise be
+// read once per head) and the heads' K chunks are loads in flight together;
+// consecutive threads take consecutive chunks of a head, so each warp's loads
+// and stores are whole 256-byte head rows.  The other CTAs copy V like
+// kv_write_kernel.  kMaxHeads bounds the K chunks one thread holds at a time;
+// a token with more kv heads takes further passes of the head loop.
+constexpr int kMaxHeads = 8;
+
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) rope_kv_write_kernel(const KvWriteParams p) {
+__global__ void __launch_bounds__(kThreads) rope_kv_write_kernel(const KvWriteParams p, unsigned k_blocks) {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     constexpr int kElemsPerChunk = BF16 ? 8 : 4;
-    const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
-    const int32_t total = 2 * per_buf;
-    const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
     const int chunks_per_head = p.head_dim / kElemsPerChunk;
+    const int n_heads = p.row_chunks / chunks_per_head;
+    if (blockIdx.x < k_blocks) {
+        const int32_t item = blockIdx.x * kThreads + threadIdx.x;   // (token, chunk offset)
+        if (item >= static_cast<int32_t>(p.n_new) * chunks_per_head) return;
+        const int32_t i = item / chunks_per_head;
+        const int c = item - i * chunks_per_head;
+        const long long loc = __ldg(p.out_cache_loc + i);
+        const int pos = __ldg(p.positions + i);
+        if (static_cast<unsigned long long>(loc) >= static_cast<unsigned long long>(p.size)) {
+            record_error(p.err, loc);
+            return;
+        }
+        if (static_cast<unsigned>(pos) >= static_cast<unsigned>(p.max_pos)) {
+            record_error(p.err, pos);
+            return;
+        }
+        const uint4 *src = static_cast<const uint4 *>(p.k) + static_cast<int64_t>(i) * p.row_chunks + c;
+        uint4 *dst = static_cast<uint4 *>(p.k_buffer) + (p.layer_row0 + loc) * p.row_chunks + c;
+        const float *cs = p.freqs_cis + (static_cast<int64_t>(pos) * (p.head_dim / 2) + c * (kElemsPerChunk / 2)) * 2;
+        for (int h0 = 0; h0 < n_heads; h0 += kMaxHeads) {
+            uint4 x[kMaxHeads];
+#pragma unroll
+            for (int h = 0; h < kMaxHeads; ++h)
+                if (h0 + h < n_heads) x[h] = __ldg(src + (h0 + h) * chunks_per_head);
+#pragma unroll
+            for (int h = 0; h < kMaxHeads; ++h)
+                if (h0 + h < n_heads)
+                    dst[(h0 + h) * chunks_per_head] = BF16 ? rotate_chunk_bf16(x[h], cs) : rotate_chunk_f32(x[h], cs);
+        }
+        return;
+    }
+    // V: a plain copy
+    const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
+    const int32_t base = (blockIdx.x - k_blocks) * (kThreads * kUnroll) + threadIdx.x;
     uint4 val[kUnroll];
     uint4 *dst[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int32_t idx = base + u * kThreads;
         dst[u] = nullptr;
-        if (idx < total) {
-            const bool is_v = idx >= per_buf;
-            const int32_t rem = is_v ? idx - per_buf : idx;
-            const int32_t i = rem / p.row_chunks;
-            const int32_t c = rem - i * p.row_chunks;
-            long long loc = __ldg(p.out_cache_loc + i);
+        if (idx < per_buf) {
+            const int32_t i = idx / p.row_chunks;
+            const int32_t c = idx - i * p.row_chunks;
+            const long long loc = __ldg(p.out_cache_loc + i);
             if (static_cast<unsigned long long>(loc) >= static_cast<unsigned long long>(p.size)) {
                 record_error(p.err, loc);
                 continue;
             }
-            uint4 x = __ldg(static_cast<const uint4 *>(is_v ? p.v : p.k) + rem);
-            if (!is_v) {
-                const int pos = __ldg(p.positions + i);
-                if (static_cast<unsigned>(pos) >= static_cast<unsigned>(p.max_pos)) {
-                    record_error(p.err, pos);
-                    continue;
-                }
-                const int pair0 = (c % chunks_per_head) * (kElemsPerChunk / 2);
-                const float *cs = p.freqs_cis + (static_cast<int64_t>(pos) * (p.head_dim / 2) + pair0) * 2;
-                x = BF16 ? rotate_chunk_bf16(x, cs) : rotate_chunk_f32(x, cs);
-            }
-            val[u] = x;
-            uint4 *buf = static_cast<uint4 *>(is_v ? p.v_buffer : p.k_buffer);
-            dst[u] = buf + (p.layer_row0 + loc) * p.row_chunks + c;
+            val[u] = __ldg(static_cast<const uint4 *>(p.v) + idx);
+            dst[u] = static_cast<uint4 *>(p.v_buffer) + (p.layer_row0 + loc) * p.row_chunks + c;
         }
     }
 #pragma unroll
@@ -165,10 +192,15 @@ cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s, bool step) {
 
 cudaError_t launch_rope_kv_write(const KvWriteParams &p, cudaStream_t s) {
     if (p.n_new == 0) return cudaSuccess;
+    const long long chunks_per_head = p.head_dim / (p.dtype == PKV_BF16 ? 8 : 4);
+    const long long k_items = p.n_new * chunks_per_head;
+    const long long v_chunks = p.n_new * p.row_chunks;
+    const unsigned k_blocks = static_cast<unsigned>((k_items + kThreads - 1) / kThreads);
+    const unsigned v_blocks = static_cast<unsigned>((v_chunks + kThreads * kUnroll - 1) / (kThreads * kUnroll));
     if (p.dtype == PKV_BF16)
-        rope_kv_write_kernel<true><<<grid_for(p), kThreads, 0, s>>>(p);
+        rope_kv_write_kernel<true><<<k_blocks + v_blocks, kThreads, 0, s>>>(p, k_blocks);
     else
-        rope_kv_write_kernel<false><<<grid_for(p), kThreads, 0, s>>>(p);
+        rope_kv_write_kernel<false><<<k_blocks + v_blocks, kThreads, 0, s>>>(p, k_blocks);
     return cudaGetLastError();
 }
 
