@@ -23,38 +23,36 @@ constexpr int kUnroll = 4;
 // carve-out at its maximum, see launch_kv_write); same code otherwise.
 template <bool kStep>
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams p) {
-    // A decode split kernel launched as a programmatic dependent of this write
-    // may start now: it reads metadata while the write runs and waits for this
-    // grid before reading K/V rows.
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
     const int32_t total = 2 * per_buf;
     const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
     uint4 val[kUnroll];
-    uint4 *dst[kUnroll];
+    long long off[kUnroll];
+    bool isv[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int32_t idx = base + u * kThreads;
-        dst[u] = nullptr;
+        off[u] = -1;
+        isv[u] = false;
         if (idx < total) {
             const bool is_v = idx >= per_buf;
             const int32_t rem = is_v ? idx - per_buf : idx;
             const int32_t i = rem / p.row_chunks;
             const int32_t c = rem - i * p.row_chunks;
-            long long loc = __ldg(p.out_cache_loc + i);
-            if (static_cast<unsigned long long>(loc) >= static_cast<unsigned long long>(p.size)) {
+            const long long loc = __ldg(p.out_cache_loc + i);
+            if (static_cast<unsigned long long>(loc) < static_cast<unsigned long long>(p.size)) {
+                val[u] = __ldg(static_cast<const uint4 *>(is_v ? p.v : p.k) + rem);
+                off[u] = (p.layer_row0 + loc) * p.row_chunks + c;
+                isv[u] = is_v;
+            } else {
                 record_error(p.err, loc);
-                continue;
             }
-            const uint4 *src = static_cast<const uint4 *>(is_v ? p.v : p.k) + rem;
-            val[u] = __ldg(src);
-            uint4 *buf = static_cast<uint4 *>(is_v ? p.v_buffer : p.k_buffer);
-            dst[u] = buf + (p.layer_row0 + loc) * p.row_chunks + c;
         }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-        if (dst[u]) *dst[u] = val[u];
+        if (off[u] >= 0) static_cast<uint4 *>(isv[u] ? p.v_buffer : p.k_buffer)[off[u]] = val[u];
 }
 
 // Rotate the pairs of one 16-byte chunk of a K row.  `pair0` is the index of
@@ -91,9 +89,12 @@ __device__ __forceinline__ uint4 rotate_chunk_f32(uint4 x, const float *cs) {
 // read once per head) and the heads' K chunks are loads in flight together;
 // consecutive threads take consecutive chunks of a head, so each warp's loads
 // and stores are whole 256-byte head rows.  The other CTAs copy V like
-// kv_write_kernel.  kMaxHeads bounds the K chunks one thread holds at a time;
-// a token with more kv heads takes further passes of the head loop.
-constexpr int kMaxHeads = 8;
+// kv_write_kernel.  A thread holds kMaxHeads K chunks at a time and takes
+// further passes of the head loop for more kv heads: the V-copy CTAs get the
+// kernel's register count too, and with 2 chunks a pass (no spills, more CTAs
+// per SM) the whole write ran 12 % faster on a 17K-token batch with 8 kv heads
+// than with all 8 chunks held at once.
+constexpr int kMaxHeads = 2;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) rope_kv_write_kernel(const KvWriteParams p, unsigned k_blocks) {
