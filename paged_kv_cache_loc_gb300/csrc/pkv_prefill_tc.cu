@@ -123,6 +123,12 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
         "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
+// descriptor from its halves (the low half holds the start address >> 4)
+__device__ __forceinline__ uint64_t desc_at(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
                  : "memory");
@@ -490,32 +496,49 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         // ================= MMA issue
         if (lane == 0) {
             const uint32_t id_s = idesc(128, 128, 0), id_o = idesc(128, D, 1);
+            // Descriptors are built once; a product's start address is a
+            // 16-byte step added to the low half (every shared address is
+            // below 2^18, so the 14-bit field cannot carry into the next).
+            const uint64_t dq = sdesc(s_base + kSmemQ, 16, 1024), dk = sdesc(s_base + kSmemK, 16, 1024);
+            const uint64_t dv = sdesc(s_base + kSmemV, 128 * 128, 1024);
+            const uint32_t q_lo = static_cast<uint32_t>(dq), q_hi = static_cast<uint32_t>(dq >> 32);
+            const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+            const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
             auto issue_s = [&](int X, int slot) {   // S_X = Q_X K^T
-                const uint32_t qaddr = s_base + kSmemQ + X * kTileBytes;
-                const uint32_t kaddr = s_base + kSmemK + slot * kTileBytes;
+                const uint32_t qa = q_lo + X * (kTileBytes >> 4), ka = k_lo + slot * (kTileBytes >> 4);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-                    mma_f16(tmem + X * 256, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + off, 16, 1024), id_s,
-                            ks > 0);
+                    const uint32_t off = ((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4;
+                    mma_f16(tmem + X * 256, desc_at(qa + off, q_hi), desc_at(ka + off, k_hi), id_s, ks > 0);
                 }
                 mma_commit(bar(kBarSFull + X));
             };
             auto issue_pv = [&](int X, int slot, bool acc) {   // O_X += P_X V; P over S_X's columns
-                const uint32_t vaddr = s_base + kSmemV + slot * kTileBytes;
+                const uint32_t va = v_lo + slot * (kTileBytes >> 4);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     // tokens [16 ks, 16 ks + 16): half ks / 4 of the row, packed at its first 32 columns
                     const uint32_t pcol = (ks >> 2) * 64 + (ks & 3) * 8;
-                    mma_f16_ta(tmem + X * 256 + 128, tmem + X * 256 + pcol,
-                               sdesc(vaddr + ks * 16 * 128, 128 * 128, 1024), id_o, (acc || ks > 0) ? 1u : 0u);
+                    mma_f16_ta(tmem + X * 256 + 128, tmem + X * 256 + pcol, desc_at(va + ks * (16 * 128 >> 4), v_hi),
+                               id_o, (acc || ks > 0) ? 1u : 0u);
                 }
             };
             auto give_up = [&](int code) {
                 *s_abort = 1;
                 record_error(p.err, code);
             };
-            bool ok = bar_wait(bar(kBarKFull), 0);
+            // Waits for the K/V ring.  The prefill's producer stores tile t
+            // once P.V_B(t - 2) has released its V slot, and each of its
+            // threads arrives on K(t) full before V(t) full, so a complete
+            // V(t) barrier means K(t) has landed too: one wait per tile,
+            // made before S(t).  The group role's producer publishes V(t)
+            // only after P.V_B(t - 1), which is issued after S(t): there S(t)
+            // waits for K(t) and P.V(t) for V(t).
+            auto wait_kv = [&](int t) -> bool {
+                const uint32_t par = (t >> 1) & 1;
+                return bar_wait(bar((kGroup ? kBarKFull : kBarVFull) + (t & 1)), par);
+            };
+            bool ok = wait_kv(0);
             if (!ok) give_up(-3002);
             if (ok) {
                 fence_after();
@@ -526,7 +549,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (*s_abort) break;
                 const bool more = j + 1 < n_tiles;
-                if (!bar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1)) { give_up(-3003); break; }
+                if (kGroup && !bar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1)) { give_up(-3003); break; }
                 if (j < n_x[0]) {
                     if (!bar_wait(bar(kBarPFull), j & 1)) { give_up(-3004); break; }
                     fence_after();
@@ -534,7 +557,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                     if (j == n_x[0] - 1) mma_commit(bar(kBarODone));
                 }
                 if (more) {
-                    if (!bar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) { give_up(-3005); break; }
+                    if (!wait_kv(j + 1)) { give_up(-3005); break; }
                     fence_after();
                     if (j + 1 < n_x[0]) issue_s(0, (j + 1) & 1);
                 }
