@@ -332,6 +332,46 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         return slot;
     };
 
+    // ---- the prefill's producer (warps 8..14) gathers K/V tile t into ring
+    // slot t % 2 through registers: the rows are mostly L2 hits here (each
+    // request's K/V is read by all its query-tile pairs), where this measured
+    // ~12% faster than the cp.async producer of the group role.  Tile t's
+    // loads go out once tile t - 1 is stored, and tile 0's while the other
+    // warps load the query tiles.
+    const bool prefill_producer = !kGroup && warp >= kSoftmaxWarps && warp < kMmaWarp;
+    const int pt = tid - kSoftmaxWarps * 32;
+    int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
+    auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
+        const int j = kv_lo + tile * kTok + pt;
+        if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
+        return slot_of(j);
+    };
+    uint4 kv[2][kChunks];   // the producer's tile in flight: K, V
+    int slot_n = 0;         // the next tile's slot index (row pt), in flight
+    auto stage_and_load = [&](int t) {
+        int *slots = s_slot + (t & 1) * kTok;
+        if (pt < kTok) slots[pt] = slot_n;
+        slot_n = fetch(t + 1);
+        named_sync(1, kPT);   // tile t's slots are staged
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            const int i = pt + k * kPT;
+            kv[0][k] = kv[1][k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < kTok * kCR) {
+                const int sl = slots[i / kCR];
+                if (sl >= 0) {
+                    const int64_t off = sl * slot_stride + (i % kCR) * 8;
+                    kv[0][k] = __ldcg(reinterpret_cast<const uint4 *>(kbase + off));
+                    kv[1][k] = __ldcg(reinterpret_cast<const uint4 *>(vbase + off));
+                }
+            }
+        }
+    };
+    if (prefill_producer) {
+        slot_n = fetch(0);
+        stage_and_load(0);
+    }
+
     // ---- setup: barriers, TMEM, the two query tiles
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
@@ -349,9 +389,12 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
-    {
+    if (!prefill_producer) {
+        // the softmax and MMA warps (all warps in the group role)
+        const int qt = kGroup ? tid : (tid < kSoftmaxWarps * 32 ? tid : tid - kPT);
+        const int qn = kGroup ? kNT : kNT - kPT;
         const bf16 *q = static_cast<const bf16 *>(p.q);
-        for (int i = tid; i < 2 * kRows * kCR; i += kNT) {
+        for (int i = qt; i < 2 * kRows * kCR; i += qn) {
             const int X = i / (kRows * kCR), rr = (i / kCR) & (kRows - 1), ch = i % kCR;
             const int Rq = row0 + X * kRows + rr;
             void *dst = sm + kSmemQ + X * kTileBytes + sw_chunk(rr, ch);
@@ -371,41 +414,13 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= kSoftmaxWarps && warp < kMmaWarp && !kGroup) {
-        // ================= producer (prefill): K and V tile t into ring slot t % 2,
-        // through registers: the rows are mostly L2 hits here (each request's
-        // K/V is read by all its query-tile pairs), where this measured ~12%
-        // faster than the cp.async producer below
-        const int pt = tid - kSoftmaxWarps * 32;
-        int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
-        auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
-            const int j = kv_lo + tile * kTok + pt;
-            if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
-            return slot_of(j);
-        };
-        int slot_n = fetch(0);
+    if (prefill_producer) {
+        // ================= producer (prefill): tile t is in registers (kv)
         // A wait that gives up sets the abort flag; after that nothing is
         // stored, but every producer barrier is still met.
+        bool live = true;
         for (int t = 0; t < n_tiles; ++t) {
-            int *slots = s_slot + (t & 1) * kTok;
-            if (pt < kTok) slots[pt] = slot_n;
-            slot_n = fetch(t + 1);   // the next tile's index is in flight meanwhile
-            named_sync(1, kPT);      // this tile's slots are staged
-            uint4 kv[2][kChunks];
-#pragma unroll
-            for (int k = 0; k < kChunks; ++k) {
-                const int i = pt + k * kPT;
-                kv[0][k] = kv[1][k] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < kTok * kCR) {
-                    const int sl = slots[i / kCR];
-                    if (sl >= 0) {
-                        const int64_t off = sl * slot_stride + (i % kCR) * 8;
-                        kv[0][k] = __ldcg(reinterpret_cast<const uint4 *>(kbase + off));
-                        kv[1][k] = __ldcg(reinterpret_cast<const uint4 *>(vbase + off));
-                    }
-                }
-            }
-            bool live = *s_abort == 0 && bar_wait(bar(kBarKEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
+            live = live && *s_abort == 0 && bar_wait(bar(kBarKEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
 #pragma unroll
             for (int X = 0; X < 2; ++X) {   // X = 0: K, 1: V
                 if (X == 1) live = live && bar_wait(bar(kBarVEmpty + (t & 1)), ((t >> 1) & 1) ^ 1);
@@ -423,6 +438,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 *s_abort = 1;
                 record_error(p.err, -2001);
             }
+            if (t + 1 < n_tiles) stage_and_load(t + 1);
         }
     } else if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
         // ================= producer (group role): K and V tile t into ring slot t % 2.
@@ -437,13 +453,6 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         // S(t - 2) and V(t) by P.V(t - 2), both of which the MMA thread can
         // issue without K(t - 1) or V(t - 1): no wait here depends on an
         // arrival that comes after it.
-        const int pt = tid - kSoftmaxWarps * 32;
-        int *s_slot = reinterpret_cast<int *>(sm + kSmemSlots);   // [2][kTok], by tile parity
-        auto fetch = [&](int tile) -> int {   // slot of row pt of `tile`, -1 past the gathered range
-            const int j = kv_lo + tile * kTok + pt;
-            if (pt >= kTok || tile >= n_tiles || j >= kv_end) return -1;
-            return slot_of(j);
-        };
         auto issue = [&](int X, int t) {   // X = 0: K, 1: V; rows past the range are zero-filled
             const int *slots = s_slot + (t & 1) * kTok;
             unsigned char *dst0 = sm + (X ? kSmemV : kSmemK) + (t & 1) * kTileBytes;
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         };
         // A wait that gives up sets the abort flag; after that nothing is
         // issued or published, but every producer barrier is still met.
-        int slot_n = fetch(0);
+        slot_n = fetch(0);
         for (int t = 0; t < n_tiles; ++t) {
             int *slots = s_slot + (t & 1) * kTok;
             if (pt < kTok) slots[pt] = slot_n;
