@@ -231,13 +231,17 @@ def test_causal_prefill_row_matches_decode_kernel():
         assert_close(f64(od)[0], f64(o)[i], "bf16", f"row {i}")
 
 
-def test_rope_kv_write():
-    case = W.make_case("rope", mode="prefill", dtype="bf16", n_layers=2, layer_id=1, size=1024,
-                       n_heads=8, n_kv_heads=4, head_dim=128, kv_lens=[40, 90], q_lens=[40, 60],
+@pytest.mark.parametrize("dtype,hq,hk,d", [("bf16", 8, 4, 128), ("bf16", 2, 1, 128), ("bf16", 6, 3, 64),
+                                            ("f32", 6, 3, 64), ("f32", 10, 5, 128)])
+def test_rope_kv_write(dtype, hq, hk, d):
+    """The fused write takes kv heads two per pass: odd and single head
+    counts leave a partial pass."""
+    case = W.make_case("rope", mode="prefill", dtype=dtype, n_layers=2, layer_id=1, size=1024,
+                       n_heads=hq, n_kv_heads=hk, head_dim=d, kv_lens=[40, 90], q_lens=[40, 60],
                        seed=123)
     rng = np.random.Generator(np.random.PCG64(5))
     max_pos = 256
-    ang = rng.uniform(-math.pi, math.pi, (max_pos, 64)).astype(np.float32)
+    ang = rng.uniform(-math.pi, math.pi, (max_pos, d // 2)).astype(np.float32)
     fc = np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32)
     pos = rng.integers(0, max_pos, case.out_cache_loc.size).astype(np.int32)
     cache, q, kn, vn = W.upload(case)
@@ -245,8 +249,15 @@ def test_rope_kv_write():
     no_device_error()
     k_rot = oracle.rope(case.k_new, fc, pos)
     got_k = f64(cache.k_buffer)[1, case.out_cache_loc]
-    # one bf16 rounding of an fp32 rotation: |err| <= 2^-8 |x| + tiny
-    assert np.all(np.abs(got_k - k_rot) <= np.abs(k_rot) * 2.0 ** -8 + 1e-6)
+    if dtype == "bf16":
+        # one bf16 rounding of an fp32 rotation: |err| <= 2^-8 |x| + tiny
+        assert np.all(np.abs(got_k - k_rot) <= np.abs(k_rot) * 2.0 ** -8 + 1e-6)
+    else:
+        # an fp32 rotation: a few fp32 roundings of terms bounded by the
+        # pair's norm, which the rotation preserves
+        x = np.asarray(case.k_new, np.float64).reshape(*case.k_new.shape[:-1], d // 2, 2)
+        norm = np.repeat(np.sqrt((x ** 2).sum(-1)), 2, axis=-1)
+        assert np.all(np.abs(got_k - k_rot) <= norm * 2.0 ** -20 + 1e-30)
     assert np.array_equal(W.host_of(cache.v_buffer)[1, case.out_cache_loc], case.v_new)
 
 
