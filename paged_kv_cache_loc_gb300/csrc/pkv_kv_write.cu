@@ -27,32 +27,34 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams 
     const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
     const int32_t total = 2 * per_buf;
     const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
+    // The row chunk and its slot are independent loads, issued together: the
+    // new rows (and slots) may sit in host memory, where each dependent round
+    // trip costs microseconds.
     uint4 val[kUnroll];
-    long long off[kUnroll];
-    bool isv[kUnroll];
+    long long loc[kUnroll];
+    int32_t rem[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int32_t idx = base + u * kThreads;
-        off[u] = -1;
-        isv[u] = false;
+        rem[u] = -1;
         if (idx < total) {
             const bool is_v = idx >= per_buf;
-            const int32_t rem = is_v ? idx - per_buf : idx;
-            const int32_t i = rem / p.row_chunks;
-            const int32_t c = rem - i * p.row_chunks;
-            const long long loc = __ldg(p.out_cache_loc + i);
-            if (static_cast<unsigned long long>(loc) < static_cast<unsigned long long>(p.size)) {
-                val[u] = __ldg(static_cast<const uint4 *>(is_v ? p.v : p.k) + rem);
-                off[u] = (p.layer_row0 + loc) * p.row_chunks + c;
-                isv[u] = is_v;
-            } else {
-                record_error(p.err, loc);
-            }
+            rem[u] = is_v ? idx - per_buf : idx;
+            loc[u] = __ldg(p.out_cache_loc + rem[u] / p.row_chunks);
+            val[u] = __ldg(static_cast<const uint4 *>(is_v ? p.v : p.k) + rem[u]);
         }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-        if (off[u] >= 0) static_cast<uint4 *>(isv[u] ? p.v_buffer : p.k_buffer)[off[u]] = val[u];
+    for (int u = 0; u < kUnroll; ++u) {
+        if (rem[u] < 0) continue;
+        if (static_cast<unsigned long long>(loc[u]) >= static_cast<unsigned long long>(p.size)) {
+            record_error(p.err, loc[u]);
+            continue;
+        }
+        const bool is_v = base + u * kThreads >= per_buf;
+        const int32_t c = rem[u] - (rem[u] / p.row_chunks) * p.row_chunks;
+        static_cast<uint4 *>(is_v ? p.v_buffer : p.k_buffer)[(p.layer_row0 + loc[u]) * p.row_chunks + c] = val[u];
+    }
 }
 
 // Rotate the pairs of one 16-byte chunk of a K row.  `pair0` is the index of
