@@ -670,19 +670,37 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
     if (n_pieces == 0) return true;
 
     const int hw = warp;   // this warp's kv head
-    auto load_q = [&](int pc, uint32_t (&qr)[D / 16][2]) {
-        const int h = lane >> 2;
-        const bf16 *qrow = static_cast<const bf16 *>(p.q) +
-                           (static_cast<int64_t>(s_b[pc]) * p.n_heads + hw * G + (h < G ? h : 0)) * D +
-                           2 * (lane & 3);
+    // q of a piece for this warp: its G query heads of the piece's entry, G x D
+    // bf16 contiguous in q (16-byte aligned).  Loaded a piece ahead with
+    // 16-byte loads -- q may sit in host memory, where a few wide requests
+    // cost far less than the mma fragment layout's 4-byte ones -- and turned
+    // into fragments through this warp's slot of shared memory at the switch.
+    constexpr int kQV = G * D / 8;         // 16-byte chunks per (piece, kv head)
+    constexpr int kQL = (kQV + 31) / 32;   // per lane
+    __shared__ __align__(16) uint4 s_q[NW][kQV];
+    auto load_q = [&](int pc, uint4 (&qr)[kQL]) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const bf16 *>(p.q) + (static_cast<int64_t>(s_b[pc]) * p.n_heads + hw * G) * D);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            qr[ks][0] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16) : 0u;
-            qr[ks][1] = h < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8) : 0u;
+        for (int j = 0; j < kQL; ++j)
+            if (lane + 32 * j < kQV) qr[j] = src[lane + 32 * j];
+    };
+    auto to_frag = [&](const uint4 (&qr)[kQL], uint32_t (&qf)[D / 16][2]) {
+        __syncwarp();   // every lane has read the previous piece's fragments
+#pragma unroll
+        for (int j = 0; j < kQL; ++j)
+            if (lane + 32 * j < kQV) s_q[warp][lane + 32 * j] = qr[j];
+        __syncwarp();
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(s_q[warp]);
+        const int h = lane >> 2;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {   // columns 16 ks + 2 (lane % 4) and + 8 of head h
+            qf[ks][0] = h < G ? w[h * (D / 2) + ks * 8 + (lane & 3)] : 0u;
+            qf[ks][1] = h < G ? w[h * (D / 2) + ks * 8 + 4 + (lane & 3)] : 0u;
         }
     };
-    uint32_t qb[D / 16][2], qn[D / 16][2];
-    load_q(0, qb);
+    uint4 q0[kQL], qn[kQL];   // the first and the next piece's q, in flight
+    load_q(0, q0);
     if (n_pieces > 1) load_q(1, qn);
 
     // stage every slot index (padding rows repeat the piece's last slot)
@@ -731,6 +749,8 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
         else cp_async_commit();
     }
 
+    uint32_t qb[D / 16][2];
+    to_frag(q0, qb);   // its loads overlapped the slot staging
     float o_acc[D / 16][4];
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
@@ -809,11 +829,8 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
         if (++pc == n_pieces) break;
         pend = (s_off[pc] + ((s_len[pc] + 15) & ~15)) >> 4;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-            qb[i][0] = qn[i][0];
-            qb[i][1] = qn[i][1];
-        }
+        for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+        to_frag(qn, qb);
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
         if (pc + 1 < n_pieces) load_q(pc + 1, qn);
