@@ -13,14 +13,16 @@
 // One CTA of 16 warps per (pair of query tiles, kv head, entry).  A query
 // tile is 128 rows of (position, head-in-group) pairs; the CTA's two tiles A
 // and B (rows [256 i, 256 i + 128) and the next 128) share every gathered
-// K/V tile, which halves the gather traffic per flop -- a gather of random
-// 256-byte rows moves only ~30 GB/s per SM even from L2, so it is what bounds
-// this kernel.  The warps specialise and hand work over through mbarriers
+// K/V tile, which halves the gathered bytes per flop: a gather of random
+// 256-byte rows beside the SM's own tensor, MUFU and TMEM traffic moves
+// ~40 GB/s per SM, and with one 64 KB tile in flight that gather sets the
+// tile period.  The warps specialise and hand work over through mbarriers
 // (every wait bounded):
 //  - producer warps 8..14 (224 threads): each 128-token K and V tile is
 //    loaded with 16-byte loads (head_dim / 8 threads per token row, slot
 //    indices staged in shared memory) into registers, then stored into a
-//    2-slot ring once the tensor core has released the slot (the group role
+//    2-slot ring once the tensor core has released the slot; tile 0 is
+//    gathered while the other warps load the query tiles (the group role
 //    copies with cp.async instead, see its producer);
 //  - MMA warp 15 (one thread) issues, per tile j,
 //      PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)     (S = Q K^T, O += P V),
