@@ -140,7 +140,13 @@ int make_plan(const pkv_kvcache *c, int32_t n_heads, int sms, const pkv_workspac
     if (chunk_req == 0 && c->kv_indptr && have_ws &&
         pkv::decode_balanced_supported(c->dtype, c->head_dim, group, c->n_kv_heads)) {
         int64_t parts = (max_len * batch + 31) / 32;   // at least ~32 tokens (2 stages) per CTA
-        const int64_t cap = sms > 0 ? sms : 1;
+        int64_t cap = sms > 0 ? sms : 1;
+        // One request with 96 to 320 positions per SM: 4/5 of the SMs, each
+        // CTA then streaming a longer piece.  Measured on GB300 (152 SMs), B=1
+        // at 16K / 32K positions: 23.8-25.2 / 35.2-35.6 us against 26.0-26.2
+        // / 35.6-36.0 us on every SM.  Shorter contexts (4K: two 16-token
+        // stages per CTA) and batched decodes measured fastest as before.
+        if (batch == 1 && max_len >= 96 * cap && max_len < 320 * cap) cap = cap * 4 / 5;
         if (parts > cap) parts = cap;
         if (parts < 1) parts = 1;
         if (ws_holds(ws, (parts + batch) * n_heads, c->head_dim)) {
