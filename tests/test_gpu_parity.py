@@ -131,6 +131,11 @@ def test_long_context_decode(ctx):
     case = W.long_decode(ctx)
     cache, q = prepare(case)
     ws = ws_for(case)
+    # the balanced plan: ~32 tokens per CTA at least, one CTA per SM at most,
+    # and 4/5 of the SMs for one request with 96 to 320 positions per SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cap = sms * 4 // 5 if 96 * sms <= ctx < 320 * sms else sms
+    assert pkv.decode_plan(cache, case.n_heads, ws) == (0, min(-(-ctx // 32), cap))
     o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
     no_device_error()
     assert_close(f64(o), oracle_decode(case), "bf16", f"ctx {ctx}")
