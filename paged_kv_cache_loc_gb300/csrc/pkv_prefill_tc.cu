@@ -767,10 +767,15 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                     st_keep(p.ml_part + unit * 2 + 1, l_row, pol);
                 }
             } else {
-                bf16 *orow = static_cast<bf16 *>(p.o) +
-                             ((static_cast<int64_t>(qo0) + pos) * p.n_heads + g * G + hh) * D + hc * (D / 2);
-                // every thread reads its lane (tcgen05.ld is warp-collective); rows
-                // past the request are not stored
+                // The warp's 32 rows x D/2 columns go through shared memory so
+                // that global stores write whole row halves (8, or 4 at head_dim
+                // 64, lanes per row) instead of one row per lane.  The staging
+                // is the first query tile's area: its last S product completed
+                // before O_A, tile B's epilogue comes after tile A's, and 16-byte
+                // chunk c of row r sits at chunk c ^ (r % kCH) (no bank conflicts).
+                constexpr int kCH = D / 16;              // 16-byte chunks per row half
+                constexpr int kRowB = D;                 // bytes per staged row half
+                unsigned char *stg = sm + kSmemQ + warp * 32 * kRowB;
 #pragma unroll
                 for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     float ov[32];
@@ -781,13 +786,31 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                         __nv_bfloat162 h = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
                         pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
                     }
-                    if (store) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4 *>(orow + c0 + q4 * 8) =
-                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int c = c0 / 8 + q4;
+                        *reinterpret_cast<uint4 *>(stg + lane * kRowB + ((c ^ (lane % kCH)) << 4)) =
+                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
                     }
                 }
+                __syncwarp();
+                if (done && *s_abort == 0) {
+                    // rows past the request are not stored
+#pragma unroll
+                    for (int i = 0; i < kCH; ++i) {
+                        const int rr = i * (32 / kCH) + lane / kCH, c = lane % kCH;
+                        const int Rr = row0 + X * kRows + (warp & 3) * 32 + rr;
+                        if (Rr < rows) {
+                            const int pr = Rr / G, hr = Rr - (Rr / G) * G;
+                            bf16 *dst = static_cast<bf16 *>(p.o) +
+                                        ((static_cast<int64_t>(qo0) + pr) * p.n_heads + g * G + hr) * D + hc * (D / 2) +
+                                        c * 8;
+                            *reinterpret_cast<uint4 *>(dst) =
+                                *reinterpret_cast<const uint4 *>(stg + rr * kRowB + ((c ^ (rr % kCH)) << 4));
+                        }
+                    }
+                }
+                __syncwarp();   // the staging rows are rewritten for the next tile
             }
         }
     }
