@@ -64,6 +64,15 @@ bool device_visible(const void *p) {
     if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
     return a.type == cudaMemoryTypeHost && a.devicePointer == p;
 }
+// Registered host memory (the kernels reach it over the host link).
+bool host_memory(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
 int check_visible(std::initializer_list<const void *> ptrs) {
     for (const void *p : ptrs)
         if (!device_visible(p)) return PKV_ERR_ARG;
@@ -486,15 +495,32 @@ int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, c
     rc = decode_prepare(c, layer_id, q, o, n_heads, sm_scale, 0, ws, &dp, &no_decode);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the tensor-core split kernels read metadata and q before waiting on
+    // the write; the others are launched in plain stream order
+    dp.pdl = !no_write && !no_decode &&
+             pkv::decode_balanced_supported(c->dtype, c->head_dim, n_heads / c->n_kv_heads, c->n_kv_heads);
+    // q in host memory: every CTA holding a piece of an entry would read the
+    // entry's q over the host link.  When the workspace has room past the
+    // partial rows this call uses, the write's extra CTAs copy q there once,
+    // and the decode reads that copy after its wait for the write.
+    if (dp.pdl && dp.balanced && c->dtype == PKV_BF16 && host_memory(q)) {
+        const int64_t rows = (static_cast<int64_t>(dp.n_parts) + c->batch) * n_heads;
+        const int64_t cap = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * ws->head_dim * 4;
+        const int64_t off = (rows * c->head_dim * 4 + 255) / 256 * 256;
+        const int64_t qbytes = static_cast<int64_t>(c->batch) * n_heads * c->head_dim * 2;
+        if (off + qbytes <= cap) {
+            wp.q_src = q;
+            wp.q_dst = reinterpret_cast<char *>(ws->o_part) + off;
+            wp.q_chunks = qbytes / 16;
+            dp.q = wp.q_dst;
+            dp.q_staged = 1;
+        }
+    }
     if (!no_write) {
         rc = map_launch(pkv::launch_kv_write(wp, s, true));
         if (rc) return rc;
     }
     if (no_decode) return PKV_OK;
-    // the tensor-core split kernels read metadata and q before waiting on
-    // the write; the others are launched in plain stream order
-    dp.pdl = !no_write && pkv::decode_balanced_supported(c->dtype, c->head_dim,
-                                                         n_heads / c->n_kv_heads, c->n_kv_heads);
     return map_launch(pkv::launch_decode(dp, c->dtype, c->head_dim, n_heads / c->n_kv_heads, s));
 }
 

@@ -700,8 +700,10 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
         }
     };
     uint4 q0[kQL], qn[kQL];   // the first and the next piece's q, in flight
-    load_q(0, q0);
-    if (n_pieces > 1) load_q(1, qn);
+    if (!p.q_staged) {   // a staged q is written by the cache write: read after the wait below
+        load_q(0, q0);
+        if (n_pieces > 1) load_q(1, qn);
+    }
 
     // stage every slot index (padding rows repeat the piece's last slot)
     for (int j = tid; j < total; j += NT) {
@@ -715,6 +717,10 @@ __device__ __forceinline__ bool stream_pieces(const DecodeParams &p, int c, long
     }
     __syncthreads();
     if (p.pdl) griddep_wait();   // K/V rows may come from the cache write before this kernel
+    if (p.q_staged) {
+        load_q(0, q0);
+        if (n_pieces > 1) load_q(1, qn);
+    }
 
     const int64_t slot_stride = static_cast<int64_t>(8) * D;
     const bf16 *kbase = static_cast<const bf16 *>(p.k_buffer) + p.layer_row0 * slot_stride;

@@ -26,6 +26,19 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvWriteParams 
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int32_t per_buf = static_cast<int32_t>(p.n_new) * p.row_chunks;
     const int32_t total = 2 * per_buf;
+    const unsigned kv_blocks = static_cast<unsigned>((total + kThreads * kUnroll - 1) / (kThreads * kUnroll));
+    if (blockIdx.x >= kv_blocks) {
+        // the CTAs past the rows copy q into the workspace (decode step)
+        const int64_t qbase = static_cast<int64_t>(blockIdx.x - kv_blocks) * (kThreads * kUnroll) + threadIdx.x;
+        uint4 qv[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (qbase + u * kThreads < p.q_chunks) qv[u] = __ldg(static_cast<const uint4 *>(p.q_src) + qbase + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (qbase + u * kThreads < p.q_chunks) static_cast<uint4 *>(p.q_dst)[qbase + u * kThreads] = qv[u];
+        return;
+    }
     const int32_t base = blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
     // The row chunk and its slot are independent loads, issued together: the
     // new rows (and slots) may sit in host memory, where each dependent round
@@ -189,7 +202,8 @@ cudaError_t launch_kv_write(const KvWriteParams &p, cudaStream_t s, bool step) {
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
-    kv_write_kernel<true><<<grid_for(p), kThreads, 0, s>>>(p);
+    const unsigned q_blocks = static_cast<unsigned>((p.q_chunks + kThreads * kUnroll - 1) / (kThreads * kUnroll));
+    kv_write_kernel<true><<<grid_for(p) + q_blocks, kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

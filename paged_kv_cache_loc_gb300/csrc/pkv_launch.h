@@ -26,6 +26,11 @@ struct KvWriteParams {
     const int32_t *positions;   // rope only: [n_new]
     int32_t max_pos;
     DevErr *err;
+    // decode step only: copy q_chunks 16-byte chunks from q_src to q_dst (q
+    // moved from host memory into the workspace once, for the decode)
+    const void *q_src;
+    void *q_dst;
+    int64_t q_chunks;
 };
 
 // Split-K paged decode.
@@ -62,6 +67,9 @@ struct DecodeParams {
     // cache write before it; it reads metadata, slot indices and q at once
     // and waits (griddepcontrol.wait) before its first K/V row read.
     int32_t pdl;
+    // 1 (with pdl): q is a copy the cache write makes in the workspace, so it
+    // is read only after the wait.
+    int32_t q_staged;
     // Page-table addressing (page_size > 0): position j of request row r is
     // slot req_to_page[r * max_pages + j / page_size] * page_size +
     // j % page_size, with pages < n_pages; req_to_token is not read.
