@@ -273,7 +273,11 @@ int pkv_paged_decode_pages(const pkv_kvcache *c, int32_t layer_id, const int32_t
  * launched as a programmatic dependent of the write: it reads kv_indptr,
  * req_pool_indices, seq_lens, req_to_token and q while the write runs and
  * waits for the write before reading K/V rows.  Those inputs therefore follow
- * plain stream order (the write never modifies them).
+ * plain stream order (the write never modifies them).  When q (bf16) is in
+ * pinned host memory and the workspace has room past the partial rows the
+ * call uses, the write also copies q into that room once, and the decode
+ * reads the copy after its wait instead of q over the host link; the result
+ * is the same either way.
  */
 int pkv_decode_step(const pkv_kvcache *c, int32_t layer_id, const void *k_new, const void *v_new,
                     int32_t n_new, const void *q, void *o, int32_t n_heads, float sm_scale,
