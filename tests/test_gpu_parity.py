@@ -858,6 +858,31 @@ def test_decode_step_reads_and_writes_pinned_host_memory():
     check_pool_bit_exact(cache, case)
 
 
+@pytest.mark.parametrize("hq,hk,d", [(8, 8, 128), (16, 8, 64), (64, 8, 128), (32, 8, 64),
+                                     (32, 4, 128), (8, 2, 64)])
+def test_decode_step_with_q_in_pinned_host_memory(hq, hk, d):
+    """q alone in pinned host memory, for every group size and head_dim of the
+    tensor-core split kernel (8 kv heads) and its piece-by-piece path (fewer kv
+    heads): the step copies q into the workspace for the decode, and o is
+    bit-identical to the step with q on the device."""
+    rng = np.random.Generator(np.random.PCG64(hq * 1000 + hk * 10 + d))
+    kv = rng.integers(1, 2500, size=12, endpoint=True)
+    case = W.make_case("q_host", mode="decode", dtype="bf16", n_layers=2, layer_id=1, size=40000,
+                       n_heads=hq, n_kv_heads=hk, head_dim=d, kv_lens=kv, seed=hq + d, rng=rng)
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    o_dev = pkv.decode_step(cache, case.layer_id, kn, vn, q, workspace=ws)
+    q_host = _pinned(case.q.view(np.int16))
+    o = torch.empty_like(o_dev)
+    pkv.decode_step(cache, case.layer_id, kn, vn, q_host, o, workspace=ws)
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(o, o_dev)
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    assert_close(f64(o), oracle_decode(case), "bf16", f"q host {hq}/{hk}/{d}")
+
+
 def test_decode_step_graph_on_pinned_host_buffers():
     """A serving loop without copies: the step captured once on pinned host
     buffers; the host rewrites q in place between replays and reads o."""
