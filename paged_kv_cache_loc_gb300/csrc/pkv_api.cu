@@ -156,6 +156,15 @@ int make_plan(const pkv_kvcache *c, int32_t n_heads, int sms, const pkv_workspac
         // / 35.6-36.0 us on every SM.  Shorter contexts (4K: two 16-token
         // stages per CTA) and batched decodes measured fastest as before.
         if (batch == 1 && max_len >= 96 * cap && max_len < 320 * cap) cap = cap * 4 / 5;
+        // A batch of fewer than 1024 positions per SM: 12/13 of the SMs (140
+        // of 152).  With every SM streaming, some SMs of a GB300 read 10-15 %
+        // slower than the rest (the same ones every call, set by the chip's
+        // layout), and a short call waits for them; with a few SMs idle the
+        // rest read evenly.  Measured on two GB300s, 32 requests x 77.7K
+        // tokens: 62.5 / 61.2 us against 65.0 / 62.5 us on every SM.  Calls
+        // of several thousand positions per SM need every SM's bandwidth
+        // (2 GB: 330 us on 152 CTAs, 353 on 140).
+        else if (batch > 1 && max_len * batch < 1024 * cap) cap = cap * 12 / 13;
         if (parts > cap) parts = cap;
         if (parts < 1) parts = 1;
         if (ws_holds(ws, (parts + batch) * n_heads, c->head_dim)) {

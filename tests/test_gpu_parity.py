@@ -112,6 +112,10 @@ def test_batched_decode_kv_write_bit_exact(batched):
 def test_batched_decode_full(batched):
     case, cache, q = batched
     ws = ws_for(case)
+    # a batch of fewer than 1024 positions per SM runs on 12/13 of the SMs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert case.max_len * case.batch < 1024 * sms
+    assert pkv.decode_plan(cache, case.n_heads, ws) == (0, sms * 12 // 13)
     o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
     no_device_error()
     assert_close(f64(o), oracle_decode(case), "bf16", "batched decode")
