@@ -121,8 +121,8 @@ int ws_check(const pkv_workspace *ws) {
 //  balanced: chosen when the caller asked for the automatic plan, passed
 //    kv_indptr, the shape has a balanced kernel and the workspace holds
 //    (n_parts + batch) * n_heads partial rows.  n_parts CTAs (one per SM, or
-//    fewer when the batch holds less than ~32 tokens per SM) share all tokens
-//    of the batch equally.
+//    fewer: when the batch holds less than ~32 tokens per SM, and in the two
+//    cases below) share all tokens of the batch equally.
 //  chunked: each entry's context is cut into chunks; about four CTAs per SM
 //    if every context were max_len long, 64..2048 tokens in steps of 32, never
 //    more splits than the workspace holds (one split without a workspace).
