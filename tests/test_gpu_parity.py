@@ -519,6 +519,35 @@ def test_decode_step_equals_write_then_decode(dtype):
     assert torch.equal(o, o2)
 
 
+def test_decode_step_new_rows_read_mid_context():
+    """A step whose new rows include slots other entries read in the middle of
+    their contexts (besides each entry's last position): the decode sees the
+    new rows there too, bit-identical to kv_write followed by paged_decode,
+    and the pool ends the same."""
+    import dataclasses
+    case = W.batched_decode(batch=16, lo=200, hi=3000, size=65536, seed=733)
+    cache, q, kn, vn = W.upload(case)
+    extra = []
+    for b, frac in ((3, 0.5), (7, 0.25), (7, 0.75), (12, 0.1), (15, 0.0)):
+        r, n = int(case.req_pool_indices[b]), int(case.seq_lens[b])
+        extra.append(int(case.req_to_token[r, int((n - 1) * frac)]))
+    rng = np.random.Generator(np.random.PCG64(12))
+    shape = (len(extra),) + tuple(kn.shape[1:])
+    bits = lambda: torch.from_numpy(W._values(rng, shape, "bf16").view(np.int16)).view(torch.bfloat16).cuda()
+    kn2, vn2 = torch.cat([kn, bits()]), torch.cat([vn, bits()])
+    loc = torch.cat([cache.out_cache_loc, torch.tensor(extra, dtype=torch.int32, device="cuda")])
+    step = dataclasses.replace(cache, out_cache_loc=loc)
+    ref = dataclasses.replace(cache, out_cache_loc=loc, k_buffer=cache.k_buffer.clone(),
+                              v_buffer=cache.v_buffer.clone())
+    o = pkv.decode_step(step, case.layer_id, kn2, vn2, q, workspace=ws_for(case, splits=64))
+    pkv.kv_write(ref, case.layer_id, kn2, vn2)
+    o_ref = pkv.paged_decode(ref, case.layer_id, q, workspace=ws_for(case, splits=64))
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(o, o_ref)
+    assert torch.equal(step.k_buffer, ref.k_buffer) and torch.equal(step.v_buffer, ref.v_buffer)
+
+
 def test_decode_step_replays_in_a_cuda_graph():
     """The step captured once (its programmatic edge becomes a graph edge),
     replayed after new K/V rows are put in the step's input buffers: the
