@@ -148,6 +148,31 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
     }
     return false;
 }
+// Packed fp32 pairs (two lanes of one 64-bit register; one instruction for
+// both): the softmax issues one instruction where it issued two.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 // 2^x with the hardware approximation (flush-to-zero); 2^-inf = 0
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -657,7 +682,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
 #pragma unroll
                 for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+                for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 7] = max3(mx[(i >> 1) & 7], sv[i], sv[i + 1]);
                 float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;   // -inf stays -inf
                 float *red = s_red + (X * 2 + (j & 1)) * 2 * kRows;
@@ -691,21 +716,29 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
                 // P = 0 (reference -inf, fma(v, scale, -inf) = -inf for finite
                 // or -inf v)
                 const float neg_m = m_run[X] == -INFINITY ? -INFINITY : -m_run[X];
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // the exponents and the row sum two lanes at a time (packed fp32)
+                const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(neg_m, neg_m);
+                uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
-                        const float p0 = ex2_approx(fmaf(sv[c * 16 + i], sc, neg_m));
-                        const float p1 = ex2_approx(fmaf(sv[c * 16 + i + 1], sc, neg_m));
-                        ls[(i >> 1) & 7] += p0 + p1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(sv[c * 16 + i], sv[c * 16 + i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        ls2[(i >> 1) & 3] = f2_add(ls2[(i >> 1) & 3], f2_pack(p0, p1));
                         __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
                         pk[i >> 1] = *reinterpret_cast<uint32_t *>(&h);
                     }
                     tmem_st8u(tS + c * 8, pk);
                 }
-                l_part[X] += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                float l0, l1, l2, l3, l4, l5, l6, l7;
+                f2_unpack(ls2[0], l0, l1);
+                f2_unpack(ls2[1], l2, l3);
+                f2_unpack(ls2[2], l4, l5);
+                f2_unpack(ls2[3], l6, l7);
+                l_part[X] += ((l0 + l1) + (l2 + l3)) + ((l4 + l5) + (l6 + l7));
                 asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
                 fence_before();
                 __syncwarp();
