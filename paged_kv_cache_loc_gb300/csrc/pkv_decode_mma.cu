@@ -380,6 +380,15 @@ struct AllHeadsCfg {
     static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0, "bulk copies move 16-byte units");
 };
 
+// 2^x by the hardware approximation (ex2.approx.ftz: one instruction;
+// results below 2^-126 flush to 0, 2^-inf = 0).  The softmax's weights are
+// then rounded to bf16, far coarser than its error.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // One 16-token block of one kv head: scores S^T = K Q^T (16 tokens x 8
 // heads), base-2 online softmax over the `valid` leading tokens (the rest
 // score -inf), O^T += V^T P^T.  kt / vt point at the block's first row in
@@ -409,11 +418,11 @@ __device__ __forceinline__ void block_math(const __nv_bfloat16 *kt, const __nv_b
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float al0 = ex2_fast(m0 - mn0), al1 = ex2_fast(m1 - mn1);
     m0 = mn0;
     m1 = mn1;
-    const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-    const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+    const float p0 = ex2_fast(s[0] - mn0), p1 = ex2_fast(s[1] - mn1);
+    const float p2 = ex2_fast(s[2] - mn0), p3 = ex2_fast(s[3] - mn1);
     l0 = l0 * al0 + p0 + p2;
     l1 = l1 * al1 + p1 + p3;
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
@@ -541,11 +550,11 @@ __device__ __forceinline__ void block_math2(const __nv_bfloat16 *kt, const __nv_
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
         const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
-        const float al0 = exp2f(m[t][0] - mn0), al1 = exp2f(m[t][1] - mn1);
+        const float al0 = ex2_fast(m[t][0] - mn0), al1 = ex2_fast(m[t][1] - mn1);
         m[t][0] = mn0;
         m[t][1] = mn1;
-        const float p0 = exp2f(s[t][0] - mn0), p1 = exp2f(s[t][1] - mn1);
-        const float p2 = exp2f(s[t][2] - mn0), p3 = exp2f(s[t][3] - mn1);
+        const float p0 = ex2_fast(s[t][0] - mn0), p1 = ex2_fast(s[t][1] - mn1);
+        const float p2 = ex2_fast(s[t][2] - mn0), p3 = ex2_fast(s[t][3] - mn1);
         l[t][0] = l[t][0] * al0 + p0 + p2;
         l[t][1] = l[t][1] * al1 + p1 + p3;
         if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
