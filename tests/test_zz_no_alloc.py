@@ -74,6 +74,43 @@ def test_noalloc_decode_matches_workspace_decode_twice(lib):
             assert err.max() <= TOL_MAX and err.mean() <= TOL_MEAN, (call, name, err.max(), err.mean())
 
 
+def test_noalloc_decode_inside_a_global_mode_capture(lib):
+    """What the entry point is for: a decode enqueued while a global-mode
+    stream capture is open (no cudaMalloc may run).  The first call, outside
+    any capture, looks up the array's address; the call is then captured in
+    a CUDA graph and replayed, and o matches the oracle."""
+    case = W.batched_decode(batch=8, lo=100, hi=2000, size=32768, seed=4343)
+    cache, q, kn, vn = W.upload(case)
+    pkv.kv_write(cache, case.layer_id, kn, vn)
+    c = cache.c_struct()
+    scale = 1.0 / math.sqrt(case.head_dim)
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    want = oracle.decode(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.seq_lens, case.q, case.layer_id, kv_indptr=case.kv_indptr)
+    o = torch.empty_like(q)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    s = ctypes.c_void_p(side.cuda_stream)
+    call = lambda: lib.pkv_paged_decode_noalloc(ctypes.byref(c), case.layer_id, ctypes.c_void_p(q.data_ptr()),
+                                                ctypes.c_void_p(o.data_ptr()), case.n_heads, scale, s)
+    assert call() == _lib.PKV_OK
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="global"):
+        assert call() == _lib.PKV_OK
+    o.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_OK, detail
+    got = _f64(o)
+    assert np.isfinite(got).all()
+    err = np.abs(got - want)
+    assert err.max() <= TOL_MAX and err.mean() <= TOL_MEAN, (err.max(), err.mean())
+
+
 def _noalloc(lib, cache, q, o, n_heads, scale):
     c = cache.c_struct()
     return lib.pkv_paged_decode_noalloc(ctypes.byref(c), 0, ctypes.c_void_p(q.data_ptr()),
