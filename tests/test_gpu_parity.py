@@ -223,6 +223,43 @@ def test_prefill_variants(heads, hk, d):
     assert_close(f64(o), ref, "bf16", "prefill variants")
 
 
+@pytest.mark.parametrize("dtype,heads,hk,d", [("bf16", 32, 16, 128), ("bf16", 32, 32, 64), ("bf16", 6, 3, 128),
+                                               ("f32", 32, 32, 64), ("f32", 48, 12, 128)])
+def test_decode_with_more_or_odd_kv_heads(dtype, heads, hk, d):
+    """kv head counts outside {1, 2, 4, 8} (3, 12, 16, 32): the decode step,
+    then the chunked plans, which also serve these counts when kv_indptr is
+    given."""
+    kv = [1, 33, 500, 2049, 130]
+    case = W.make_case("kvh", mode="decode", dtype=dtype, n_layers=2, layer_id=1, size=8192,
+                       n_heads=heads, n_kv_heads=hk, head_dim=d, kv_lens=kv, seed=515)
+    cache, q, kn, vn = W.upload(case)
+    ws = ws_for(case, splits=64)
+    o = pkv.decode_step(cache, case.layer_id, kn, vn, q, workspace=ws)
+    no_device_error()
+    oracle.kv_write(case.k_buffer, case.v_buffer, case.layer_id, case.k_new, case.v_new,
+                    case.out_cache_loc)
+    check_pool_bit_exact(cache, case)
+    ref = oracle_decode(case)
+    assert_close(f64(o), ref, dtype, "decode step")
+    for chunk in (0, 64, 2048):
+        o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws, chunk=chunk)
+        no_device_error()
+        assert_close(f64(o), ref, dtype, f"chunk {chunk}")
+
+
+@pytest.mark.parametrize("heads,hk,d", [(32, 16, 128), (32, 32, 64), (6, 3, 128), (48, 12, 64)])
+def test_prefill_with_more_or_odd_kv_heads(heads, hk, d):
+    q_lens = [1, 65, 130, 300]
+    pre = [0, 7, 100, 513]
+    case = W.make_case("kvh_pre", mode="prefill", dtype="bf16", n_layers=2, layer_id=1, size=8192,
+                       n_heads=heads, n_kv_heads=hk, head_dim=d,
+                       kv_lens=[a + b for a, b in zip(q_lens, pre)], q_lens=q_lens, seed=516)
+    _, _, o = run_prefill(case)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id)
+    assert_close(f64(o), ref, "bf16", f"prefill hk={hk}")
+
+
 def test_causal_prefill_row_matches_decode_kernel():
     """Prefill row i (prefix P) and decode at context P+i+1 agree on the GPU."""
     case = W.make_case("cross", mode="prefill", dtype="bf16", n_layers=2, layer_id=0, size=2048,
@@ -405,6 +442,25 @@ def test_balanced_decode_long_ranges():
     o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
     no_device_error()
     assert_close(f64(o), oracle_decode(case), "bf16", "long ranges")
+
+
+def test_single_context_of_half_a_million_positions():
+    """B=1 at 524,295 positions (1 GB of bf16 K/V rows): the balanced plan
+    gives every CTA more than 2048 positions, and the chunked plan (no
+    kv_indptr) cuts the context into host-chosen chunks."""
+    ctx = 524295
+    case = W.make_case("b1_max", mode="decode", dtype="bf16", n_layers=1, layer_id=0, size=ctx,
+                       n_heads=32, n_kv_heads=8, head_dim=128, kv_lens=[ctx], seed=77, max_ctx_len=ctx)
+    cache, q = prepare(case)
+    ref = oracle_decode(case)
+    ws = ws_for(case, splits=1024)
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), ref, "bf16", "balanced")
+    cache.kv_indptr = None
+    o = pkv.paged_decode(cache, case.layer_id, q, workspace=ws)
+    no_device_error()
+    assert_close(f64(o), ref, "bf16", "chunked")
 
 
 def test_workspace_too_small_is_rejected():
