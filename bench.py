@@ -144,8 +144,9 @@ def run_profile_case(which: str) -> None:
         cache, q, kn, vn = W.upload(case)
         pkv.kv_write(cache, case.layer_id, kn, vn)
         o = torch.empty_like(q)
+        ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1)   # entries longest first
         for _ in range(2):
-            pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o)
+            pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o, workspace=ws)
     else:
         case = W.ragged_prefill()
         cache, q, kn, vn = W.upload(case)
@@ -756,13 +757,15 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
     case = W.ragged_prefill()
     cache, q, kn, vn = W.upload(case, dev)
     o = torch.empty_like(q)
+    # a workspace lets the prefill take its entries longest first
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1, device=dev)
 
     def write():
         pkv.kv_write(cache, case.layer_id, kn, vn, stream=stream)
 
     def attend():
         pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o,
-                          stream=stream)
+                          workspace=ws, stream=stream)
     # the fused RoPE write of the same rows: standard rotary table
     # (theta = 10000^(-2i/d), [max_pos, d/2, 2] f32), each new token at its
     # position P + i in its request
@@ -814,9 +817,11 @@ def prefill_d64_leg(torch, pkv, W, stream, flush, peaks, args, dev):
     cache, q, kn, vn = W.upload(case, dev)
     pkv.kv_write(cache, case.layer_id, kn, vn, stream=stream)
     o = torch.empty_like(q)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1, device=dev)
     with torch.cuda.stream(stream):
         ms, _ = timed(torch, stream, lambda: pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len,
-                                                              case.max_len, o=o, stream=stream),
+                                                              case.max_len, o=o, workspace=ws,
+                                                              stream=stream),
                       args.prefill_steps, 3, flush)
     st, detail = pkv.last_device_error(stream, dev)
     if st != 0:

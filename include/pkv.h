@@ -315,8 +315,15 @@ int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *
  * sizing).  An entry whose rows [qo_indptr[b], qo_indptr[b+1]) do not lie
  * within [0, qo_indptr[batch]), or whose lengths break these bounds, is a
  * device-data error: its rows of q and o are neither read nor written.
- * `ws` may be NULL.  Supported: bf16, head_dim 64 or 128 (5th-generation
- * tensor cores, accumulators in tensor memory), G in {1, 2, 4, 8}.
+ * `ws` may be NULL.  With a workspace (pkv_workspace_init; its o_part must
+ * hold 8 ints per entry) and 2 to 256 entries, a one-CTA planning kernel
+ * checks the entries and ranks them by decreasing kv_len into the start of
+ * o_part, and the prefill, launched as its programmatic dependent, takes the
+ * entries in that order: the longest start first and the short ones fill
+ * the SMs at the end.  The result is the same bits in either order.  The
+ * workspace serves one call at a time (as for the decode).  Supported: bf16,
+ * head_dim 64 or 128 (5th-generation tensor cores, accumulators in tensor
+ * memory), G in {1, 2, 4, 8}.
  */
 int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
                       int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,

@@ -559,7 +559,6 @@ int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *
 int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, void *o,
                       int32_t n_heads, int32_t max_q_len, int32_t max_kv_len, int32_t causal,
                       float sm_scale, const pkv_workspace *ws, void *stream) {
-    (void)ws;
     int rc = check_pool(c, layer_id);
     if (rc) return rc;
     rc = check_attn(c, n_heads, q, o);
@@ -576,8 +575,12 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
     DeviceInfo di;
     rc = device_info(&di);
     if (rc) return rc;
+    if (ws) {
+        rc = ws_check(ws);
+        if (rc) return rc;
+    }
     rc = check_visible({c->k_buffer, c->v_buffer, c->req_to_token, c->req_pool_indices, c->qo_indptr,
-                        c->kv_indptr, q, o});
+                        c->kv_indptr, q, o, ws ? ws->base : nullptr});
     if (rc) return rc;
     pkv::PrefillParams p{};
     p.q = q;
@@ -600,6 +603,10 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
     p.max_kv_len = max_kv_len;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.err = di.err;
+    if (ws) {   // room for the entry order: 8 ints per entry at the start of o_part
+        const int64_t cap = static_cast<int64_t>(ws->max_batch) * ws->n_heads * ws->max_splits * ws->head_dim;
+        if (8LL * c->batch <= cap) p.plan = reinterpret_cast<int32_t *>(ws->o_part);
+    }
     return map_launch(pkv::launch_prefill(p, c->dtype, c->head_dim, group,
                                           static_cast<cudaStream_t>(stream)));
 }

@@ -127,6 +127,10 @@ struct PrefillParams {
     int32_t max_kv_len;
     float scale_log2;
     DevErr *err;
+    // With a workspace: 8 ints per entry rank (entry, request row, first
+    // packed row, q_len, kv_len, valid, 0, 0), the entries by decreasing
+    // kv_len, written by the plan kernel that runs first; CTA z takes rank z.
+    int32_t *plan;
     // Shared-prefix group role (launch_shared_group_tc), not used by the
     // prefill: rows are the batch x G (entry, head) pairs of q [batch,
     // n_heads, head_dim]; the keys are positions [0, shared_len) of the
@@ -147,6 +151,7 @@ struct PrefillParams {
 
 constexpr int kDecodeMaxChunk = 2048;   // slot indices staged per split (or per piece)
 constexpr int kDecodeMaxSplits = 1024;  // merge kernel limit
+constexpr int kPlanMaxBatch = 256;      // prefill entries ordered by the plan kernel (one CTA)
 
 // Each returns cudaSuccess or the launch error.  Unsupported variants return
 // cudaErrorNotSupported and enqueue nothing.

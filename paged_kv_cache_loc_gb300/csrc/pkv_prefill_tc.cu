@@ -246,6 +246,51 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
 }
+// The order in which the prefill takes its entries, when the caller gives a
+// workspace.  The hardware hands CTAs to SMs in launch order, and a CTA's
+// work grows with its entry's kv_len (each of its query-tile pairs streams up
+// to kv_len / 128 key tiles), so launching the entries by decreasing kv_len
+// makes the list schedule longest first: the short entries fill the SMs at
+// the end instead of a long one starting last.  One CTA: thread t checks
+// entry t as the prefill kernel would (a failure is recorded here and the
+// entry is ranked last, with no work), ranks it by (kv_len descending, entry
+// ascending) against all entries, and writes its row of the table.  The
+// prefill kernel is launched as this kernel's programmatic dependent and
+// reads its row after griddepcontrol.wait.
+constexpr int kPlanThreads = kPlanMaxBatch;
+
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PrefillParams p) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    __shared__ int s_key[kPlanThreads];
+    const int t = threadIdx.x;
+    int r = 0, qo0 = 0, q_len = 0, kv_len = 0, key = -1;
+    if (t < p.batch) {
+        r = __ldg(p.req_pool_indices + t);
+        qo0 = __ldg(p.qo_indptr + t);
+        q_len = __ldg(p.qo_indptr + t + 1) - qo0;
+        kv_len = __ldg(p.kv_indptr + t + 1) - __ldg(p.kv_indptr + t);
+        const long long q_total = __ldg(p.qo_indptr + p.batch);
+        const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
+        if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
+            q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len)
+            record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
+                                : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
+        else
+            key = kv_len;
+    }
+    s_key[t] = key;
+    __syncthreads();
+    if (t >= p.batch) return;
+    int rank = 0;
+    for (int e = 0; e < p.batch; ++e) {
+        const int k = s_key[e];
+        rank += k > key || (k == key && e < t);
+    }
+    int4 *row = reinterpret_cast<int4 *>(p.plan + 8 * rank);
+    row[0] = make_int4(t, r, qo0, q_len);
+    row[1] = make_int4(kv_len, key >= 0 ? 1 : 0, 0, 0);
+}
+
 // kGroup = false: the ragged prefill, one CTA per (query-tile pair, kv head,
 // entry).  kGroup = true: the group role of a shared-prefix decode, one CTA
 // per (chunk of the shared prefix, kv head, 256 query rows): the rows are the
@@ -292,22 +337,35 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         kv_end = min(p.shared_len, kv_lo + p.chunk_len);
         lim_pos = kv_end - 1;
     } else {
-        const int b = blockIdx.z;
-        qp = gridDim.x - 1 - blockIdx.x;   // longest causal work first
-        r = __ldg(p.req_pool_indices + b);
-        qo0 = __ldg(p.qo_indptr + b);
-        const int q_len = __ldg(p.qo_indptr + b + 1) - qo0;
-        const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-        // q and o hold qo_indptr[batch] packed rows: this entry's rows must lie
-        // inside them, or they are neither read nor written
-        const long long q_total = __ldg(p.qo_indptr + p.batch);
-        const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
-        if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
-            q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
-            if (qp == 0 && g == 0 && tid == 0)
-                record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
-                                    : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
-            return;
+        qp = gridDim.x - 1 - blockIdx.x;   // longest causal work of the entry first
+        int q_len, kv_len;
+        if (p.plan) {
+            // the entry of rank blockIdx.z, longest first (checked by the plan kernel)
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            const int4 *row = reinterpret_cast<const int4 *>(p.plan) + 2 * blockIdx.z;
+            const int4 e0 = __ldcg(row), e1 = __ldcg(row + 1);
+            if (!e1.y) return;
+            r = e0.y;
+            qo0 = e0.z;
+            q_len = e0.w;
+            kv_len = e1.x;
+        } else {
+            const int b = blockIdx.z;
+            r = __ldg(p.req_pool_indices + b);
+            qo0 = __ldg(p.qo_indptr + b);
+            q_len = __ldg(p.qo_indptr + b + 1) - qo0;
+            kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+            // q and o hold qo_indptr[batch] packed rows: this entry's rows must
+            // lie inside them, or they are neither read nor written
+            const long long q_total = __ldg(p.qo_indptr + p.batch);
+            const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
+            if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
+                q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
+                if (qp == 0 && g == 0 && tid == 0)
+                    record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
+                                        : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
+                return;
+            }
         }
         rows = q_len * G;
         P = kv_len - q_len;
@@ -880,9 +938,26 @@ cudaError_t run(const PrefillParams &p, cudaStream_t s) {
     cudaError_t e = set_smem_once<G, false, D>();
     if (e != cudaSuccess) return e;
     const int qtiles = (p.max_q_len * G + kRows - 1) / kRows;
-    dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
-    prefill_tc_kernel<G, false, D><<<grid, kNT, TcLayout<D>::kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    const dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
+    if (!p.plan) {
+        prefill_tc_kernel<G, false, D><<<grid, kNT, TcLayout<D>::kSmemBytes, s>>>(p);
+        return cudaGetLastError();
+    }
+    // the entry order first; the prefill as its programmatic dependent
+    prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kNT);
+    cfg.dynamicSmemBytes = TcLayout<D>::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G, false, D>, p);
 }
 
 template <int D>
@@ -950,7 +1025,9 @@ bool prefill_supported(int dtype, int head_dim, int group) {
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, int head_dim, int group, cudaStream_t s) {
     if (!prefill_supported(dtype, head_dim, group)) return cudaErrorNotSupported;
     if (p.batch == 0 || p.max_q_len == 0) return cudaSuccess;
-    return head_dim == 128 ? run_d<128>(p, group, s) : run_d<64>(p, group, s);
+    PrefillParams q = p;
+    if (q.batch < 2 || q.batch > kPlanMaxBatch) q.plan = nullptr;
+    return head_dim == 128 ? run_d<128>(q, group, s) : run_d<64>(q, group, s);
 }
 
 cudaError_t launch_shared_group_tc(const DecodeParams &p, int group, cudaStream_t s) {

@@ -170,6 +170,52 @@ def test_ragged_prefill_reduced_full_check(causal, d):
     assert_close(f64(o), ref, "bf16", "reduced prefill")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_with_a_workspace_takes_entries_longest_first(causal):
+    """With a workspace a planning kernel orders the entries by decreasing
+    kv_len and the prefill takes them in that order: the same bits as batch
+    order, equal to the oracle, also replayed from a CUDA graph."""
+    case = W.ragged_prefill(batch=12, q_lo=1, q_hi=300, p_hi=700, size=16384, seed=2011)
+    cache, q = prepare(case)
+    o0 = pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, causal=causal)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1)
+    o1 = pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, causal=causal,
+                           workspace=ws)
+    no_device_error()
+    assert torch.equal(o0, o1)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id, causal=causal)
+    assert_close(f64(o1), ref, "bf16", "prefill with a workspace")
+    o2 = torch.full_like(q, float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, causal=causal, o=o2,
+                          workspace=ws, stream=side)
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(o0, o2)
+
+
+def test_prefill_with_a_workspace_beyond_the_planned_batch():
+    """More entries than the planning kernel orders (256): batch order, still
+    equal to the oracle."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    q_lens = rng.integers(0, 4, 300)
+    kv = q_lens + rng.integers(0, 40, 300)
+    case = W.make_case("plan_big", mode="prefill", dtype="bf16", n_layers=1, layer_id=0, size=16384,
+                       n_heads=8, n_kv_heads=2, head_dim=128, kv_lens=kv, q_lens=q_lens, seed=13)
+    cache, q = prepare(case)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1)
+    o = pkv.paged_prefill(cache, 0, q, case.max_q_len, case.max_len, workspace=ws)
+    no_device_error()
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, 0)
+    assert_close(f64(o), ref, "bf16", "300 entries")
+
+
 def test_ragged_prefill_full_size_sampled():
     case = W.ragged_prefill()
     cache, q, o = run_prefill(case)
@@ -362,8 +408,8 @@ def test_device_data_errors_are_reported_not_faulted(hk, indptr):
     assert_close(f64(o), oracle_decode(case), "bf16", "after errors")
 
 
-@pytest.mark.parametrize("d", [128, 64])
-def test_prefill_rows_outside_q_are_reported_not_touched(d):
+@pytest.mark.parametrize("d,with_ws", [(128, False), (64, False), (128, True)])
+def test_prefill_rows_outside_q_are_reported_not_touched(d, with_ws):
     """A qo_indptr entry whose packed rows fall outside [0, qo_indptr[batch])
     is recorded and its rows are neither read nor written.  q and o are
     views into buffers padded by 64 rows on each side, so that even an
@@ -382,8 +428,9 @@ def test_prefill_rows_outside_q_are_reported_not_touched(d):
                           req_to_token=cache.req_to_token, req_pool_indices=cache.req_pool_indices,
                           kv_indptr=cache.kv_indptr, max_len=case.max_len,
                           qo_indptr=torch.tensor(qo, dtype=torch.int32, device="cuda"))
+        ws = pkv.Workspace(case.batch, case.n_heads, d, 1) if with_ws else None
         pkv.paged_prefill(bad, case.layer_id, qp[pad:pad + q.shape[0]], 40, case.max_len,
-                          o=op[pad:pad + q.shape[0]])
+                          o=op[pad:pad + q.shape[0]], workspace=ws)
         assert pkv.last_device_error()[0] == _lib.PKV_ERR_INDEX
         assert torch.all(op[:pad] == 7.0) and torch.all(op[-pad:] == 7.0), "padding was written"
     # the context is still healthy and the word was cleared
