@@ -312,7 +312,9 @@ int pkv_decode_plan(const pkv_kvcache *c, int32_t n_heads, const pkv_workspace *
  * visible), else j < kv_len, reading slot req_to_token[req_pool_indices[b], j]
  * of kv head h / G.  q, o: [qo_indptr[batch], n_heads, head_dim] bf16.
  * max_q_len / max_kv_len: host-side upper bounds of q_len and kv_len (grid
- * sizing).  An entry whose rows [qo_indptr[b], qo_indptr[b+1]) do not lie
+ * sizing; max_q_len * G at most 65535 * 256 rows, else PKV_ERR_ARG).  The
+ * CTAs launch the kv heads of a query-tile pair together, the pairs of an
+ * entry longest first, then the entries.  An entry whose rows [qo_indptr[b], qo_indptr[b+1]) do not lie
  * within [0, qo_indptr[batch]), or whose lengths break these bounds, is a
  * device-data error: its rows of q and o are neither read nor written.
  * `ws` may be NULL.  With a workspace (pkv_workspace_init; its o_part must

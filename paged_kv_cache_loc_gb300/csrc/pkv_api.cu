@@ -572,6 +572,7 @@ int pkv_paged_prefill(const pkv_kvcache *c, int32_t layer_id, const void *q, voi
     if (c->batch == 0 || max_q_len == 0) return PKV_OK;
     if (q == o) return PKV_ERR_ARG;
     if (static_cast<int64_t>(max_q_len) * group / 64 + 1 > INT32_MAX) return PKV_ERR_ARG;
+    if ((static_cast<int64_t>(max_q_len) * group + 255) / 256 > 65535) return PKV_ERR_ARG;   // grid y: query-tile pairs
     DeviceInfo di;
     rc = device_info(&di);
     if (rc) return rc;

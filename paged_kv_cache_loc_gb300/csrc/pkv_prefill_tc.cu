@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
     auto bar = [&](int i) -> uint32_t { return s_base + kSmemBar + 8 * i; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y;
+    // The prefill launches the kv heads of one query-tile pair next to each
+    // other (x), then the pairs (y, longest first), then the entries (z): the
+    // CTAs running at once read the same token rows, each its head's part.
+    const int g = kGroup ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
     int qp, r, qo0, rows, kv_lo = 0, chunk = 0;
     int n_x[2], kv_end = 0;
     int lim_pos = 0;   // group: last key position of the chunk
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         kv_end = min(p.shared_len, kv_lo + p.chunk_len);
         lim_pos = kv_end - 1;
     } else {
-        qp = gridDim.x - 1 - blockIdx.x;   // longest causal work of the entry first
+        qp = gridDim.y - 1 - blockIdx.y;   // longest causal work of the entry first
         int q_len, kv_len;
         if (p.plan) {
             // the entry of rank blockIdx.z, longest first (checked by the plan kernel)
@@ -938,7 +941,7 @@ cudaError_t run(const PrefillParams &p, cudaStream_t s) {
     cudaError_t e = set_smem_once<G, false, D>();
     if (e != cudaSuccess) return e;
     const int qtiles = (p.max_q_len * G + kRows - 1) / kRows;
-    const dim3 grid((qtiles + 1) / 2, p.n_kv_heads, p.batch);   // two query tiles per CTA
+    const dim3 grid(p.n_kv_heads, (qtiles + 1) / 2, p.batch);   // two query tiles per CTA, heads fastest
     if (!p.plan) {
         prefill_tc_kernel<G, false, D><<<grid, kNT, TcLayout<D>::kSmemBytes, s>>>(p);
         return cudaGetLastError();
