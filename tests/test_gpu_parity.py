@@ -199,6 +199,30 @@ def test_prefill_with_a_workspace_takes_entries_longest_first(causal):
     assert torch.equal(o0, o2)
 
 
+@pytest.mark.parametrize("with_ws", [False, True])
+def test_prefill_entry_with_a_bad_request_row_leaves_the_others_exact(with_ws):
+    """One entry's request row lies outside req_to_token: it is recorded, its
+    rows of o are not written, and every other entry still matches the
+    oracle, in batch order and in the planned order."""
+    case = W.ragged_prefill(batch=6, q_lo=1, q_hi=200, p_hi=400, size=8192, seed=2013)
+    cache, q = prepare(case)
+    ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
+                         case.qo_indptr, case.kv_indptr, case.q, case.layer_id)
+    rpi = case.req_pool_indices.copy()
+    rpi[2] = case.num_reqs + 5
+    cache.req_pool_indices = torch.from_numpy(rpi).cuda()
+    o = torch.full_like(q, 7.0)
+    ws = pkv.Workspace(case.batch, case.n_heads, case.head_dim, 1) if with_ws else None
+    pkv.paged_prefill(cache, case.layer_id, q, case.max_q_len, case.max_len, o=o, workspace=ws)
+    st, detail = pkv.last_device_error()
+    assert st == _lib.PKV_ERR_INDEX and detail == case.num_reqs + 5
+    got = f64(o)
+    lo, hi = int(case.qo_indptr[2]), int(case.qo_indptr[3])
+    assert np.all(got[lo:hi] == 7.0), "the bad entry's rows were written"
+    keep = np.r_[0:lo, hi:got.shape[0]]
+    assert_close(got[keep], ref[keep], "bf16", "the other entries")
+
+
 def test_prefill_with_a_workspace_beyond_the_planned_batch():
     """More entries than the planning kernel orders (256): batch order, still
     equal to the oracle."""
