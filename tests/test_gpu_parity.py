@@ -223,12 +223,14 @@ def test_prefill_entry_with_a_bad_request_row_leaves_the_others_exact(with_ws):
     assert_close(got[keep], ref[keep], "bf16", "the other entries")
 
 
-def test_prefill_with_a_workspace_beyond_the_planned_batch():
-    """More entries than the planning kernel orders (256): batch order, still
-    equal to the oracle."""
-    rng = np.random.Generator(np.random.PCG64(12))
-    q_lens = rng.integers(0, 4, 300)
-    kv = q_lens + rng.integers(0, 40, 300)
+@pytest.mark.parametrize("batch", [2, 256, 257, 300])
+def test_prefill_with_a_workspace_at_the_planned_batch_limits(batch):
+    """2 and 256 entries are ordered by the planning kernel, 257 and more run
+    in batch order: all equal to the oracle, and the same bits as without a
+    workspace."""
+    rng = np.random.Generator(np.random.PCG64(12 + batch))
+    q_lens = rng.integers(0, 4, batch)
+    kv = q_lens + rng.integers(0, 40, batch)
     case = W.make_case("plan_big", mode="prefill", dtype="bf16", n_layers=1, layer_id=0, size=16384,
                        n_heads=8, n_kv_heads=2, head_dim=128, kv_lens=kv, q_lens=q_lens, seed=13)
     cache, q = prepare(case)
@@ -237,7 +239,8 @@ def test_prefill_with_a_workspace_beyond_the_planned_batch():
     no_device_error()
     ref = oracle.prefill(case.k_buffer, case.v_buffer, case.req_to_token, case.req_pool_indices,
                          case.qo_indptr, case.kv_indptr, case.q, 0)
-    assert_close(f64(o), ref, "bf16", "300 entries")
+    assert_close(f64(o), ref, "bf16", f"{batch} entries")
+    assert torch.equal(o, pkv.paged_prefill(cache, 0, q, case.max_q_len, case.max_len))
 
 
 def test_ragged_prefill_full_size_sampled():
