@@ -340,7 +340,6 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         kv_end = min(p.shared_len, kv_lo + p.chunk_len);
         lim_pos = kv_end - 1;
     } else {
-        qp = gridDim.y - 1 - blockIdx.y;   // longest causal work of the entry first
         int q_len, kv_len;
         if (p.plan) {
             // the entry of rank blockIdx.z, longest first (checked by the plan kernel)
@@ -364,7 +363,7 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
             const bool rows_ok = qo0 >= 0 && static_cast<long long>(qo0) + q_len <= q_total;
             if (static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) || q_len < 0 || !rows_ok ||
                 q_len > p.max_q_len || kv_len < q_len || kv_len > p.max_ctx_len || kv_len > p.max_kv_len) {
-                if (qp == 0 && g == 0 && tid == 0)
+                if (blockIdx.y == 0 && g == 0 && tid == 0)
                     record_error(p.err, static_cast<unsigned>(r) >= static_cast<unsigned>(p.num_reqs) ? r
                                         : (q_len >= 0 && !rows_ok) ? qo0 : kv_len);
                 return;
@@ -373,6 +372,9 @@ __global__ void __launch_bounds__(kNT, 1) prefill_tc_kernel(const PrefillParams 
         rows = q_len * G;
         P = kv_len - q_len;
         lim_pos = kv_len - 1;
+        // the entry's pairs longest first, then the grid's spare pairs (no rows)
+        qp = (rows + 2 * kRows - 1) / (2 * kRows) - 1 - static_cast<int>(blockIdx.y);
+        if (qp < 0) return;
     }
     const int row0 = qp * 2 * kRows;
     if (row0 >= rows || kv_end - kv_lo < 0) return;
