@@ -792,6 +792,7 @@ def prefill_leg(torch, pkv, W, stream, flush, peaks, args, dev):
     wb = kv_write_bytes(case)
     rb = wb + float(pos.size) * (4 + (d // 2) * 2 * 4)   # + position and table row per token
     return {"workload": "ragged causal prefill", "total_q": int(case.q_lens.sum()),
+            "launch_order": "kv heads of a query-tile pair together; entries by decreasing kv_len (planning kernel, workspace given)",
             "causal_flops": fl, "ms_prefill": round(t_attn, 4),
             "tflops": round(tf, 1), "roofline": {
                 "bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
